@@ -1,0 +1,206 @@
+"""CPU oracle for the CODA GEMM-epilogue block -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA product path never does.
+
+What it computes is the *plain, unfused* definition of the block that the CODA
+news write-ups reparameterise ("CODA: the treasure hidden in the epilogue"):
+
+    h  = R + X.W1                          first GEMM + residual add
+    r  = 1 / sqrt(mean_j h_j^2 + eps)      RMSNorm row scale
+    y  = h * r * gamma                     RMSNorm output (LLaMA form)
+    Z  = y.W2                              second GEMM
+ or act = silu(y.Wg) * (y.Wu)               SwiGLU gate/up ("five blocks":
+                                           elementwise activation)
+
+The GPU path computes the reparameterised form (diag(r) moved past the second
+GEMM, gamma folded into its weight); the oracle deliberately does not, so that
+the two meet only in their results.  All arithmetic is fp64 in the C file
+``coda_oracle.c``; this module only marshals numpy arrays and composes the
+steps in the order the block applies them.
+
+Parity pins (tests/test_oracle.py): hand-derived 4x4 cases and a one-row chain
+in tests/golden/, numpy fp64 matmul on a C0-sized case, the reparameterisation
+identity, RMSNorm scale invariance, silu special values, and the E4M3 codec
+against torch's float8_e4m3fn over all 256 codes.
+
+Weights are passed in the mathematical orientation W [K, N] (``nn.Linear``'s
+weight transposed).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "coda_oracle.c")
+_LIB = os.path.join(_HERE, "libcoda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP; no -ffast-math, no -march)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.coda_oracle_gemm.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64]
+            lib.coda_oracle_rmsnorm.argtypes = [_dp, _dp, ctypes.c_double, _i64, _i64, _dp, _dp]
+            lib.coda_oracle_silu.argtypes = [ctypes.c_double]
+            lib.coda_oracle_silu.restype = ctypes.c_double
+            lib.coda_oracle_silu_mul.argtypes = [_dp, _dp, _i64, _dp]
+            lib.coda_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.coda_oracle_e4m3_decode.restype = ctypes.c_double
+            lib.coda_oracle_e4m3_encode.argtypes = [ctypes.c_double]
+            lib.coda_oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.coda_oracle_amax.argtypes = [_dp, _i64]
+            lib.coda_oracle_amax.restype = ctypes.c_double
+            lib.coda_oracle_e4m3_fake_quant.argtypes = [_dp, _i64, _dp]
+            lib.coda_oracle_e4m3_fake_quant.restype = ctypes.c_double
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    if hasattr(a, "detach"):  # torch tensor: widen its exact bits
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+# ---------------------------------------------------------------- steps ----
+
+def gemm(A, W, R=None) -> np.ndarray:
+    """C = R + A.W (R optional).  A [M,K], W [K,N]."""
+    A, W = _f64(A), _f64(W)
+    M, K = A.shape
+    K2, N = W.shape
+    assert K == K2, (A.shape, W.shape)
+    C = np.empty((M, N), dtype=np.float64)
+    Rp = None
+    if R is not None:
+        R = _f64(R)
+        assert R.shape == (M, N)
+        Rp = _ptr(R)
+    _load().coda_oracle_gemm(_ptr(A), _ptr(W), Rp, _ptr(C), M, N, K)
+    return C
+
+
+def rmsnorm(H, gamma, eps: float):
+    """Returns (y, rstd) with rstd_i = 1/sqrt(mean_j h_ij^2 + eps), y = h*rstd*gamma."""
+    H, gamma = _f64(H), _f64(gamma)
+    M, N = H.shape
+    Y = np.empty_like(H)
+    rstd = np.empty(M, dtype=np.float64)
+    _load().coda_oracle_rmsnorm(_ptr(H), _ptr(gamma), float(eps), M, N, _ptr(Y), _ptr(rstd))
+    return Y, rstd
+
+
+def silu(x: float) -> float:
+    return _load().coda_oracle_silu(float(x))
+
+
+def silu_mul(G, U) -> np.ndarray:
+    G, U = _f64(G), _f64(U)
+    assert G.shape == U.shape
+    out = np.empty_like(G)
+    _load().coda_oracle_silu_mul(_ptr(G), _ptr(U), G.size, _ptr(out))
+    return out
+
+
+def swiglu(Y, Wg, Wu) -> np.ndarray:
+    """act = silu(Y.Wg) * (Y.Wu)."""
+    return silu_mul(gemm(Y, Wg), gemm(Y, Wu))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().coda_oracle_e4m3_encode(float(x)))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(_load().coda_oracle_e4m3_decode(int(code)))
+
+
+def fake_quant_e4m3(x):
+    """Per-tensor E4M3 quantise-dequantise with s = amax/448.  Returns (x~, s)."""
+    x = _f64(x)
+    out = np.empty_like(x)
+    s = _load().coda_oracle_e4m3_fake_quant(_ptr(x), x.size, _ptr(out))
+    return out, s
+
+
+# --------------------------------------------------------------- blocks ----
+
+def block_rowscale(X, W1, R, gamma, W2, eps):
+    """GEMM -> residual add -> RMSNorm -> GEMM, unfused."""
+    h = gemm(X, W1, R)
+    y, rstd = rmsnorm(h, gamma, eps)
+    return {"h": h, "r": rstd, "Z": gemm(y, W2)}
+
+
+def block_swiglu(X, W1, R, gamma, Wg, Wu, eps):
+    """GEMM -> residual add -> RMSNorm -> gate/up GEMMs -> SwiGLU, unfused."""
+    h = gemm(X, W1, R)
+    y, rstd = rmsnorm(h, gamma, eps)
+    return {"h": h, "r": rstd, "act": swiglu(y, Wg, Wu)}
+
+
+def chain_full(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps):
+    """Pre-norm LLaMA block tail and the next layer's QKV projection:
+    h1 = R + X.Wo ; y1 = RMSNorm(h1) ; act = SwiGLU(y1) ; h2 = h1 + act.Wd ;
+    y2 = RMSNorm(h2) ; Z = y2.Wq."""
+    h1 = gemm(X, Wo, R)
+    y1, r1 = rmsnorm(h1, gamma1, eps)
+    act = swiglu(y1, Wg, Wu)
+    h2 = gemm(act, Wd, h1)
+    y2, r2 = rmsnorm(h2, gamma2, eps)
+    return {"h1": h1, "r1": r1, "act": act, "h2": h2, "r2": r2, "Z": gemm(y2, Wq)}
+
+
+def chain_full_fp8(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps):
+    """Quantisation-aware FP8 chain.  FP8 changes the arithmetic, so here the
+    oracle follows the reparameterised steps and quantises exactly the GEMM
+    operands an FP8 implementation feeds the tensor cores: X, every weight
+    (gamma folded in first), h1, act and h2, each with its own per-tensor
+    scale amax/448.  R, h, r and the outputs stay unquantised."""
+    q = lambda t: fake_quant_e4m3(t)[0]
+    g1, g2 = _f64(gamma1), _f64(gamma2)
+    Wg_f = _f64(Wg) * g1[:, None]
+    Wu_f = _f64(Wu) * g1[:, None]
+    Wq_f = _f64(Wq) * g2[:, None]
+    h1 = gemm(q(X), q(Wo), R)
+    _, r1 = rmsnorm(h1, g1, eps)
+    h1q = q(h1)
+    G = gemm(h1q, q(Wg_f)) * r1[:, None]
+    U = gemm(h1q, q(Wu_f)) * r1[:, None]
+    act = silu_mul(G, U)
+    h2 = gemm(q(act), q(Wd), h1)
+    _, r2 = rmsnorm(h2, g2, eps)
+    Z = gemm(q(h2), q(Wq_f)) * r2[:, None]
+    return {"h1": h1, "r1": r1, "act": act, "h2": h2, "r2": r2, "Z": Z}
+
+
+def rel_err(got, ref) -> float:
+    """max |got - ref| / (max |ref| + 1e-6): the parity metric of the block."""
+    got, ref = _f64(got), _f64(ref)
+    return float(np.max(np.abs(got - ref)) / (np.max(np.abs(ref)) + 1e-6)) if ref.size else 0.0

@@ -1,0 +1,191 @@
+"""Pins for the CPU oracle: checks against values and facts that do not come
+from the oracle itself (hand-derived golden cases, numpy's fp64 matmul, the
+reparameterisation identity of the CODA write-ups, RMSNorm's scale
+invariance, closed forms of silu, torch's float8_e4m3fn codec)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tiny_blocks.json")))
+A = np.asarray
+
+
+def _close(got, want, tol=1e-12):
+    got, want = A(got, dtype=np.float64), A(want, dtype=np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    np.testing.assert_allclose(got, want, rtol=tol, atol=tol)
+
+
+@pytest.mark.parametrize("case", [c for c in GOLDEN["cases"] if c["kind"] == "rowscale"],
+                         ids=lambda c: c["name"])
+def test_golden_rowscale(case):
+    out = oracle.block_rowscale(A(case["X"]), A(case["W1"]), A(case["R"]), A(case["gamma"]),
+                                A(case["W2"]), case["eps"])
+    _close(out["h"], case["h"])
+    _close(out["r"], case["r"])
+    _close(out["Z"], case["Z"])
+
+
+def test_golden_full_chain():
+    c = next(c for c in GOLDEN["cases"] if c["kind"] == "full")
+    args = [A(c[k]) for k in ("X", "Wo", "R", "gamma1", "Wg", "Wu", "Wd", "gamma2", "Wq")]
+    for fn in (oracle.chain_full, oracle.chain_full_fp8):
+        # every tensor of this case is exactly representable after per-tensor
+        # E4M3 scaling (a single nonzero magnitude per tensor), so the
+        # quantisation-aware chain must reproduce the exact values too
+        out = fn(*args, c["eps"])
+        for k in ("h1", "r1", "act", "h2", "r2", "Z"):
+            _close(out[k], c[k], 1e-12)
+
+
+def test_golden_swiglu_gate_vs_up():
+    c = GOLDEN["swiglu_gate_up"]
+    _close(oracle.swiglu(A(c["Y"]), A(c["Wg"]), A(c["Wu"])), c["act"])
+
+
+def test_silu_closed_forms():
+    for x, want in GOLDEN["silu"]["points"]:
+        assert oracle.silu(x) == pytest.approx(want, rel=1e-15, abs=1e-300)
+    # silu(x) -> x for large x, -> 0 (from below) for very negative x
+    assert oracle.silu(40.0) == pytest.approx(40.0, rel=1e-15)
+    assert -1e-15 < oracle.silu(-40.0) < 0.0
+    # silu(x) - silu(-x) = x (sigmoid(x) + sigmoid(-x) = 1)
+    for x in (0.3, 1.7, 5.0):
+        assert oracle.silu(x) - oracle.silu(-x) == pytest.approx(x, rel=1e-14)
+
+
+def test_gemm_matches_numpy_fp64():
+    rng = np.random.default_rng(0)
+    X = rng.standard_normal((256, 512))
+    W = rng.standard_normal((512, 384)) / math.sqrt(512)
+    R = rng.standard_normal((256, 384))
+    np.testing.assert_allclose(oracle.gemm(X, W), X @ W, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.gemm(X, W, R), R + X @ W, rtol=1e-12, atol=1e-12)
+
+
+def test_rmsnorm_matches_closed_form_on_random_rows():
+    rng = np.random.default_rng(1)
+    H = rng.standard_normal((7, 33)) * 3.0
+    g = 1.0 + 0.1 * rng.standard_normal(33)
+    y, r = oracle.rmsnorm(H, g, 1e-5)
+    for i in range(7):
+        want_r = 1.0 / math.sqrt(sum(v * v for v in H[i]) / 33 + 1e-5)
+        assert r[i] == pytest.approx(want_r, rel=1e-13)
+        np.testing.assert_allclose(y[i], H[i] * want_r * g, rtol=1e-13)
+
+
+def test_reparameterisation_identity():
+    """RMSNorm(h).gamma.W2 == diag(r) . h . (diag(gamma) W2): the row scale
+    commutes with the next matmul ('the treasure hidden in the epilogue')."""
+    rng = np.random.default_rng(2)
+    M, K, N, N2 = 256, 512, 512, 384
+    X = rng.standard_normal((M, K))
+    R = rng.standard_normal((M, N))
+    W1 = rng.standard_normal((K, N)) / math.sqrt(K)
+    W2 = rng.standard_normal((N, N2)) / math.sqrt(N)
+    g = 1.0 + 0.1 * rng.standard_normal(N)
+    out = oracle.block_rowscale(X, W1, R, g, W2, 1e-6)
+    reparam = out["r"][:, None] * (out["h"] @ (g[:, None] * W2))
+    np.testing.assert_allclose(out["Z"], reparam, rtol=1e-11, atol=1e-11)
+    # SwiGLU with the row scale applied to both projections before silu
+    Wg = rng.standard_normal((N, 96)) / math.sqrt(N)
+    Wu = rng.standard_normal((N, 96)) / math.sqrt(N)
+    sw = oracle.block_swiglu(X, W1, R, g, Wg, Wu, 1e-6)
+    G = out["r"][:, None] * (out["h"] @ (g[:, None] * Wg))
+    U = out["r"][:, None] * (out["h"] @ (g[:, None] * Wu))
+    np.testing.assert_allclose(sw["act"], G / (1 + np.exp(-G)) * U, rtol=1e-11, atol=1e-11)
+
+
+def test_scale_invariance():
+    """eps=0: scaling a row of h by c>0 leaves RMSNorm's output unchanged and
+    divides r by c."""
+    rng = np.random.default_rng(3)
+    M, K, N = 8, 32, 48
+    X, R = rng.standard_normal((M, K)), rng.standard_normal((M, N))
+    W1, W2 = rng.standard_normal((K, N)), rng.standard_normal((N, 16))
+    g = 1.0 + 0.1 * rng.standard_normal(N)
+    base = oracle.block_rowscale(X, W1, R, g, W2, 0.0)
+    c = np.array([1.0, 2.0, 0.5, 50.0, 1e-3, 7.0, 1.0, 3.0])
+    sc = oracle.block_rowscale(X * c[:, None], W1, R * c[:, None], g, W2, 0.0)
+    np.testing.assert_allclose(sc["h"], base["h"] * c[:, None], rtol=1e-12)
+    np.testing.assert_allclose(sc["r"], base["r"] / c, rtol=1e-12)
+    np.testing.assert_allclose(sc["Z"], base["Z"], rtol=1e-10, atol=1e-12)
+    # constant row (a, ..., a) with eps=0 normalises to sign(a) * gamma
+    y, _ = oracle.rmsnorm(np.full((2, 5), [[-2.5], [4.0]]), np.arange(1.0, 6.0), 0.0)
+    np.testing.assert_allclose(y, [[-1, -2, -3, -4, -5], [1, 2, 3, 4, 5]], rtol=1e-14)
+
+
+def test_e4m3_decode_all_codes_vs_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.nanmax(got) == 448.0 and np.nanmin(np.abs(got[got != 0])) == 2.0 ** -9
+
+
+def test_e4m3_encode_vs_torch_rne():
+    rng = np.random.default_rng(4)
+    x = np.concatenate([rng.standard_normal(4000) * s for s in (1e-3, 0.05, 1.0, 30.0, 150.0)])
+    x = x[np.abs(x) <= 448.0]
+    # all midpoints between neighbouring codes: ties go to the even code
+    vals = np.array(sorted(set(oracle.e4m3_decode(c) for c in range(0, 0x7F))))
+    mids = (vals[1:] + vals[:-1]) / 2
+    x = np.concatenate([x, mids, -mids, vals, -vals])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(v) for v in x], dtype=np.uint8)
+    # -0.0 / +0.0 may differ only in sign bit for inputs that round to zero
+    zero = (ref & 0x7F) == 0
+    assert np.array_equal(got[~zero], ref[~zero])
+    assert np.all((got[zero] & 0x7F) == 0)
+
+
+def test_e4m3_saturates_and_nan():
+    assert oracle.e4m3_encode(448.0) == 0x7E
+    assert oracle.e4m3_encode(470.0) == 0x7E      # would round to 480: saturate
+    assert oracle.e4m3_encode(1e30) == 0x7E
+    assert oracle.e4m3_encode(-1e30) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) & 0x7F == 0x7F
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00  # tie between 0 and 2^-9: even
+    assert oracle.e4m3_encode(3 * 2.0 ** -10) == 0x02
+
+
+def test_fake_quant_exact_on_representable_and_bounded_error():
+    vals = np.array([oracle.e4m3_decode(c) for c in range(0, 0x7F)])
+    s = 0.125
+    x = np.concatenate([vals, -vals]) * s
+    xq, sq = oracle.fake_quant_e4m3(x)
+    assert sq == pytest.approx(448.0 * s / 448.0)
+    np.testing.assert_array_equal(xq, x)
+    rng = np.random.default_rng(5)
+    y = rng.standard_normal(10000)
+    yq, sy = oracle.fake_quant_e4m3(y)
+    normal = np.abs(y) >= sy * 2.0 ** -6
+    # relative rounding error of a normal E4M3 number is at most 2^-4
+    assert np.max(np.abs(yq - y)[normal] / np.abs(y[normal])) <= 2.0 ** -4 + 1e-12
+
+
+def test_fp8_chain_close_to_exact_chain():
+    rng = np.random.default_rng(6)
+    M, H, I, Q = 16, 64, 96, 48
+    X, R = rng.standard_normal((M, H)), rng.standard_normal((M, H))
+    Wo, Wg, Wu = (rng.standard_normal(s) / math.sqrt(s[0]) for s in ((H, H), (H, I), (H, I)))
+    Wd, Wq = rng.standard_normal((I, H)) / math.sqrt(I), rng.standard_normal((H, Q)) / math.sqrt(H)
+    g1, g2 = 1 + 0.1 * rng.standard_normal(H), 1 + 0.1 * rng.standard_normal(H)
+    ex = oracle.chain_full(X, Wo, R, g1, Wg, Wu, Wd, g2, Wq, 1e-5)
+    q8 = oracle.chain_full_fp8(X, Wo, R, g1, Wg, Wu, Wd, g2, Wq, 1e-5)
+    for k in ("h1", "act", "h2", "Z"):
+        e = oracle.rel_err(q8[k], ex[k])
+        assert 1e-4 < e < 0.1, (k, e)   # quantisation is visible but bounded
+
+
+def test_rel_err_metric():
+    assert oracle.rel_err([1.0, 2.0], [1.0, 2.0]) == 0.0
+    assert oracle.rel_err([1.0, 2.5], [1.0, 2.0]) == pytest.approx(0.25, rel=1e-6)
