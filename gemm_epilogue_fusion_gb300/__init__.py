@@ -1,0 +1,218 @@
+"""Python binding of the GB300 fused GEMM-epilogue library (``include/coda.h``).
+
+Argument marshalling only: every function here takes torch tensors, checks
+that they are contiguous CUDA tensors, passes their device pointers, sizes and
+the current CUDA stream to the C ABI function of the same name, and raises
+``CodaError`` on a non-OK status.  All arithmetic runs in the library's
+kernels; PyTorch only provides device memory and streams.  Outputs can be
+passed in (pre-allocated) or are allocated with ``torch.empty``.
+
+The library is ``libcoda_gb300.so`` next to this file, compiled for sm_103a
+by ``_build.build()``.  There is no fallback: if it cannot be built or
+loaded, importing a function raises.
+
+Hot path (the CODA write-up, section "CODA: the treasure hidden in the
+epilogue"):
+
+    h, P = coda_gemm_residual_partial_rms(X, W1t, R)   # h = R + X W1, partial sums of h^2
+    r    = coda_rms_reduce(P, N, eps)                  # r = 1/sqrt(mean h^2 + eps)
+    Z    = coda_gemm_rowscale(h, W2t_folded, r)        # diag(r) h diag(gamma) W2
+    act  = coda_gemm_swiglu(h, Wgt_folded, Wut_folded, r)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+CODA_OK, CODA_ERR_INVALID_ARG, CODA_ERR_UNSUPPORTED, CODA_ERR_CUDA, CODA_ERR_TIMEOUT = range(5)
+CODA_F32, CODA_BF16, CODA_E4M3 = 0, 1, 2
+
+_STATUS_NAMES = {0: "CODA_OK", 1: "CODA_ERR_INVALID_ARG", 2: "CODA_ERR_UNSUPPORTED", 3: "CODA_ERR_CUDA",
+                 4: "CODA_ERR_TIMEOUT"}
+
+# Every symbol include/coda.h declares, with (restype, argtypes).
+_vp, _fp, _i64, _i32, _f32 = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "coda_version": (_i32, []),
+    "coda_status_string": (ctypes.c_char_p, [_i32]),
+    "coda_last_error": (ctypes.c_char_p, []),
+    "coda_partial_cols": (_i64, [_i64]),
+    "coda_fold_gamma": (_i32, [_vp, _fp, _vp, _i64, _i64, _i32, _vp]),
+    "coda_gemm_residual_partial_rms": (_i32, [_vp, _vp, _vp, _vp, _fp, _i64, _i64, _i64, _i32, _fp, _fp, _fp, _vp]),
+    "coda_rms_reduce": (_i32, [_fp, _i64, _i64, _f32, _fp, _vp]),
+    "coda_gemm_rowscale": (_i32, [_vp, _vp, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _vp]),
+    "coda_gemm_swiglu": (_i32, [_vp, _vp, _vp, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _fp, _fp, _vp]),
+    "coda_amax": (_i32, [_vp, _i64, _i32, _fp, _vp]),
+    "coda_quantize_e4m3": (_i32, [_vp, _i64, _i32, _fp, _vp, _fp, _vp]),
+    "coda_get_device_status": (_i32, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CodaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libcoda_gb300.so (compiling it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build_if_missing else _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library {path} is missing: run __graft_entry__.build()")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype, fn.argtypes = res, args
+            _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != CODA_OK:
+        raise CodaError(status, load_library().coda_last_error().decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return CODA_F32
+    if t.dtype == torch.bfloat16:
+        return CODA_BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return CODA_E4M3
+    raise TypeError(f"unsupported operand dtype {t.dtype}")
+
+
+def _out_dtype(code: int) -> torch.dtype:
+    return torch.float32 if code == CODA_F32 else torch.bfloat16
+
+
+def _dev(t: Optional[torch.Tensor], name: str):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr() or None
+
+
+def _stream(t: torch.Tensor, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def coda_partial_cols(N: int) -> int:
+    return int(load_library().coda_partial_cols(N))
+
+
+def coda_fold_gamma(Wt: torch.Tensor, gamma: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
+    """W'^T = W^T diag(gamma): out[n, k] = Wt[n, k] * gamma[k]."""
+    lib = load_library()
+    N_out, K = Wt.shape
+    out = torch.empty_like(Wt) if out is None else out
+    _check(lib.coda_fold_gamma(_dev(Wt, "Wt"), _dev(gamma, "gamma"), _dev(out, "out"), N_out, K, _dtype_code(Wt),
+                               _stream(Wt, stream)))
+    return out
+
+
+def coda_gemm_residual_partial_rms(X, W1t, R, H=None, P=None, *, scale_x=None, scale_w=None, amax_h=None,
+                                   stream=None):
+    """h = R + X W1 (W1t = W1^T) and P[i, g] = sum of h[i, j]^2 over 128-column group g.  Returns (h, P)."""
+    lib = load_library()
+    M, K = X.shape
+    N = W1t.shape[0]
+    code = _dtype_code(X)
+    if H is None:
+        H = torch.empty(M, N, dtype=_out_dtype(code), device=X.device)
+    if P is None:
+        P = torch.empty(M, max(coda_partial_cols(N), 0), dtype=torch.float32, device=X.device)
+    _check(lib.coda_gemm_residual_partial_rms(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(H, "H"),
+                                              _dev(P, "P"), M, N, K, code, _dev(scale_x, "scale_x"),
+                                              _dev(scale_w, "scale_w"), _dev(amax_h, "amax_h"), _stream(X, stream)))
+    return H, P
+
+
+def coda_rms_reduce(P, N: int, eps: float, r=None, stream=None):
+    """r[i] = 1 / sqrt(sum_g P[i, g] / N + eps)."""
+    lib = load_library()
+    M = P.shape[0]
+    if r is None:
+        r = torch.empty(M, dtype=torch.float32, device=P.device)
+    _check(lib.coda_rms_reduce(_dev(P, "P"), M, N, float(eps), _dev(r, "r"), _stream(P, stream)))
+    return r
+
+
+def coda_gemm_rowscale(H, W2t, r, Z=None, *, scale_h=None, scale_w=None, stream=None):
+    """Z = diag(r) H W2 (W2t = W2^T, gamma already folded in)."""
+    lib = load_library()
+    M, K = H.shape
+    N2 = W2t.shape[0]
+    code = _dtype_code(H)
+    if Z is None:
+        Z = torch.empty(M, N2, dtype=_out_dtype(code), device=H.device)
+    _check(lib.coda_gemm_rowscale(_dev(H, "H"), _dev(W2t, "W2t"), _dev(r, "r"), _dev(Z, "Z"), M, N2, K, code,
+                                  _dev(scale_h, "scale_h"), _dev(scale_w, "scale_w"), _stream(H, stream)))
+    return Z
+
+
+def coda_gemm_swiglu(H, Wgt, Wut, r=None, Act=None, *, scale_h=None, scale_wg=None, scale_wu=None, amax_act=None,
+                     stream=None):
+    """Act = silu(diag(r) H Wg) * (diag(r) H Wu)."""
+    lib = load_library()
+    M, K = H.shape
+    I = Wgt.shape[0]
+    code = _dtype_code(H)
+    if Act is None:
+        Act = torch.empty(M, I, dtype=_out_dtype(code), device=H.device)
+    _check(lib.coda_gemm_swiglu(_dev(H, "H"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"), _dev(r, "r"), _dev(Act, "Act"),
+                                M, I, K, code, _dev(scale_h, "scale_h"), _dev(scale_wg, "scale_wg"),
+                                _dev(scale_wu, "scale_wu"), _dev(amax_act, "amax_act"), _stream(H, stream)))
+    return Act
+
+
+def coda_amax(x, amax=None, stream=None):
+    """amax = max |x| (fp32 scalar tensor)."""
+    lib = load_library()
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib.coda_amax(_dev(x, "x"), x.numel(), _dtype_code(x), _dev(amax, "amax"), _stream(x, stream)))
+    return amax
+
+
+def coda_quantize_e4m3(x, amax, q=None, scale=None, stream=None):
+    """q = e4m3(x / s) with s = amax / 448; returns (q as uint8, s)."""
+    lib = load_library()
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib.coda_quantize_e4m3(_dev(x, "x"), x.numel(), _dtype_code(x), _dev(amax, "amax"), _dev(q, "q"),
+                                  _dev(scale, "scale"), _stream(x, stream)))
+    return q, scale
+
+
+def coda_get_device_status() -> int:
+    """Synchronise and read/clear the device status word; raises CodaError on a timeout."""
+    st = load_library().coda_get_device_status()
+    _check(st)
+    return st

@@ -1,0 +1,112 @@
+"""The CODA blocks as sequences of C-ABI calls (no arithmetic here).
+
+Each function enqueues the block's kernels on the current CUDA stream and
+returns its outputs; ``bufs`` lets a caller (the benchmark) pass the output
+tensors of a previous call back in so that nothing is allocated per step.
+
+Blocks (the CODA write-up, section "CODA: the treasure hidden in the
+epilogue"; SwiGLU gate/up from the same section and "five blocks"):
+  rowscale_block  h = R + X W1 ; r ; Z = diag(r) h W2'            (3 launches)
+  swiglu_block    h = R + X W1 ; r ; act = silu(r h Wg') (r h Wu') (3 launches)
+  full_chain      LLaMA block tail and the next layer's QKV projection:
+                  h1 = R + X Wo ; r1 ; act = SwiGLU(r1, h1) ;
+                  h2 = h1 + act Wd ; r2 ; Z = diag(r2) h2 Wq'          (6 launches)
+  full_chain_fp8  the same with every GEMM operand in per-tensor-scaled e4m3
+W' = diag(gamma) W is prepared once by ``fold_weights`` (coda_fold_gamma).
+Weights are W^T [N_out, K] row-major throughout.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import torch
+
+from . import (coda_amax, coda_fold_gamma, coda_gemm_residual_partial_rms, coda_gemm_rowscale, coda_gemm_swiglu,
+               coda_quantize_e4m3, coda_rms_reduce)
+
+
+def _b(bufs, key):
+    return None if bufs is None else bufs.get(key)
+
+
+def fold_weights(chain: str, W: Dict[str, torch.Tensor], gammas: Dict[str, torch.Tensor]) -> Dict[str, torch.Tensor]:
+    """Fold each RMSNorm weight into the GEMM that follows its norm."""
+    out = dict(W)
+    if chain == "rowscale":
+        out["W2t"] = coda_fold_gamma(W["W2t"], gammas["gamma1"])
+    elif chain == "swiglu":
+        out["Wgt"] = coda_fold_gamma(W["Wgt"], gammas["gamma1"])
+        out["Wut"] = coda_fold_gamma(W["Wut"], gammas["gamma1"])
+    elif chain == "full":
+        out["Wgt"] = coda_fold_gamma(W["Wgt"], gammas["gamma1"])
+        out["Wut"] = coda_fold_gamma(W["Wut"], gammas["gamma1"])
+        out["Wqt"] = coda_fold_gamma(W["Wqt"], gammas["gamma2"])
+    else:
+        raise ValueError(chain)
+    return out
+
+
+def rowscale_block(X, W1t, R, W2t_folded, eps: float, bufs: Optional[dict] = None) -> dict:
+    h, P = coda_gemm_residual_partial_rms(X, W1t, R, _b(bufs, "h"), _b(bufs, "P"))
+    r = coda_rms_reduce(P, W1t.shape[0], eps, _b(bufs, "r"))
+    Z = coda_gemm_rowscale(h, W2t_folded, r, _b(bufs, "Z"))
+    return {"h": h, "P": P, "r": r, "Z": Z}
+
+
+def swiglu_block(X, W1t, R, Wgt_folded, Wut_folded, eps: float, bufs: Optional[dict] = None) -> dict:
+    h, P = coda_gemm_residual_partial_rms(X, W1t, R, _b(bufs, "h"), _b(bufs, "P"))
+    r = coda_rms_reduce(P, W1t.shape[0], eps, _b(bufs, "r"))
+    act = coda_gemm_swiglu(h, Wgt_folded, Wut_folded, r, _b(bufs, "act"))
+    return {"h": h, "P": P, "r": r, "act": act}
+
+
+def full_chain(X, Wot, R, Wgt_f, Wut_f, Wdt, Wqt_f, eps: float, bufs: Optional[dict] = None) -> dict:
+    H = Wot.shape[0]
+    h1, P1 = coda_gemm_residual_partial_rms(X, Wot, R, _b(bufs, "h1"), _b(bufs, "P1"))
+    r1 = coda_rms_reduce(P1, H, eps, _b(bufs, "r1"))
+    act = coda_gemm_swiglu(h1, Wgt_f, Wut_f, r1, _b(bufs, "act"))
+    h2, P2 = coda_gemm_residual_partial_rms(act, Wdt, h1, _b(bufs, "h2"), _b(bufs, "P2"))
+    r2 = coda_rms_reduce(P2, H, eps, _b(bufs, "r2"))
+    Z = coda_gemm_rowscale(h2, Wqt_f, r2, _b(bufs, "Z"))
+    return {"h1": h1, "P1": P1, "r1": r1, "act": act, "h2": h2, "P2": P2, "r2": r2, "Z": Z}
+
+
+def quantize_weights(W: Dict[str, torch.Tensor]) -> Dict[str, tuple]:
+    """Per-tensor e4m3 copies (q, scale) of already-folded weights."""
+    out = {}
+    for k, w in W.items():
+        out[k] = coda_quantize_e4m3(w, coda_amax(w))
+    return out
+
+
+def full_chain_fp8(X, R, Wq8: Dict[str, tuple], eps: float, bufs: Optional[dict] = None) -> dict:
+    """FP8 chain: X, h1, act, h2 quantised per tensor on the device (amax of
+    h1, act and h2 comes out of the producing GEMM's epilogue); weights from
+    ``quantize_weights`` (keys Wot, Wgt, Wut, Wdt, Wqt, gamma folded)."""
+    b = bufs if bufs is not None else {}
+    dev = X.device
+    for k in ("ax", "a1", "a2", "a3"):
+        if k not in b:
+            b[k] = torch.empty(1, dtype=torch.float32, device=dev)
+    Wo, so = Wq8["Wot"]
+    Wg, sg = Wq8["Wgt"]
+    Wu, su = Wq8["Wut"]
+    Wd, sd = Wq8["Wdt"]
+    Wq, sq = Wq8["Wqt"]
+    H = Wo.shape[0]
+    coda_amax(X, b["ax"])
+    Xq, sx = coda_quantize_e4m3(X, b["ax"], b.get("Xq"), b.get("sx"))
+    h1, P1 = coda_gemm_residual_partial_rms(Xq, Wo, R, b.get("h1"), b.get("P1"), scale_x=sx, scale_w=so,
+                                            amax_h=b["a1"])
+    r1 = coda_rms_reduce(P1, H, eps, b.get("r1"))
+    h1q, s1 = coda_quantize_e4m3(h1, b["a1"], b.get("h1q"), b.get("s1"))
+    act = coda_gemm_swiglu(h1q, Wg, Wu, r1, b.get("act"), scale_h=s1, scale_wg=sg, scale_wu=su, amax_act=b["a2"])
+    actq, s2 = coda_quantize_e4m3(act, b["a2"], b.get("actq"), b.get("s2"))
+    h2, P2 = coda_gemm_residual_partial_rms(actq, Wd, h1, b.get("h2"), b.get("P2"), scale_x=s2, scale_w=sd,
+                                            amax_h=b["a3"])
+    r2 = coda_rms_reduce(P2, H, eps, b.get("r2"))
+    h2q, s3 = coda_quantize_e4m3(h2, b["a3"], b.get("h2q"), b.get("s3"))
+    Z = coda_gemm_rowscale(h2q, Wq, r2, b.get("Z"), scale_h=s3, scale_w=sq)
+    b.update({"Xq": Xq, "sx": sx, "h1": h1, "P1": P1, "r1": r1, "h1q": h1q, "s1": s1, "act": act, "actq": actq,
+              "s2": s2, "h2": h2, "P2": P2, "r2": r2, "h2q": h2q, "s3": s3, "Z": Z})
+    return b

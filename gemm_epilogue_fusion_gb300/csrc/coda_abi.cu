@@ -1,0 +1,417 @@
+// C ABI of the fused GEMM-epilogue library: argument validation, dispatch to
+// the kernel translation units, error reporting.  Nothing here allocates or
+// synchronises (except coda_get_device_status, which says so).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cinttypes>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "coda.h"
+#include "coda_internal.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+coda_status fail(coda_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+coda_status fail(coda_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+coda_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(CODA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int elem_bytes(coda_dtype d) { return d == CODA_F32 ? 4 : d == CODA_BF16 ? 2 : 1; }
+// residual / output element size for GEMMs with this operand type
+int out_bytes(coda_dtype d) { return d == CODA_F32 ? 4 : 2; }
+bool valid_dtype(int d) { return d == CODA_F32 || d == CODA_BF16 || d == CODA_E4M3; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  const char* name;
+  uintptr_t lo, hi;  // [lo, hi)
+};
+Range rng(const char* name, const void* p, int64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {name, a, a + static_cast<uintptr_t>(bytes)};
+}
+bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+// Every output range against every input range and every other output.
+coda_status check_overlaps(const Range* outs, int n_out, const Range* ins, int n_in) {
+  for (int i = 0; i < n_out; ++i) {
+    for (int j = 0; j < n_in; ++j)
+      if (overlap(outs[i], ins[j]))
+        return fail(CODA_ERR_INVALID_ARG, "output %s overlaps input %s", outs[i].name, ins[j].name);
+    for (int j = i + 1; j < n_out; ++j)
+      if (overlap(outs[i], outs[j]))
+        return fail(CODA_ERR_INVALID_ARG, "outputs %s and %s overlap", outs[i].name, outs[j].name);
+  }
+  return CODA_OK;
+}
+
+#define REQUIRE(cond, ...)                                 \
+  do {                                                     \
+    if (!(cond)) return fail(CODA_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+coda_status check_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(CODA_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(CODA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return CODA_OK;
+}
+
+coda_status check_scalar_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(CODA_ERR_INVALID_ARG, "%s is NULL", name);
+  if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0) return fail(CODA_ERR_INVALID_ARG, "%s is not 4-byte aligned", name);
+  return CODA_OK;
+}
+
+#define TRY(expr)                        \
+  do {                                   \
+    coda_status s_ = (expr);             \
+    if (s_ != CODA_OK) return s_;        \
+  } while (0)
+
+// Shape rules common to the GEMM calls.
+coda_status check_gemm_dims(int64_t M, int64_t N, int64_t K, coda_dtype dt, const char* nname) {
+  REQUIRE(valid_dtype(dt), "unknown dtype %d", static_cast<int>(dt));
+  REQUIRE(M >= 0 && M < INT32_MAX, "M = %" PRId64 " out of range [0, 2^31)", M);
+  REQUIRE(N > 0 && N < INT32_MAX, "%s = %" PRId64 " out of range [1, 2^31)", nname, N);
+  REQUIRE(K > 0 && K < INT32_MAX, "K = %" PRId64 " out of range [1, 2^31)", K);
+  REQUIRE((K * elem_bytes(dt)) % 16 == 0, "K = %" PRId64 " must be a multiple of %d for this dtype (16-byte rows)", K,
+          16 / elem_bytes(dt));
+  REQUIRE((N * out_bytes(dt)) % 16 == 0, "%s = %" PRId64 " must be a multiple of %d for this dtype (16-byte rows)",
+          nname, N, 16 / out_bytes(dt));
+  return CODA_OK;
+}
+
+coda_status check_scales(coda_dtype dt, const float* a, const char* an, const float* b, const char* bn,
+                         const float* c = nullptr, const char* cn = nullptr) {
+  if (dt == CODA_E4M3) {
+    TRY(check_scalar_ptr(a, an));
+    TRY(check_scalar_ptr(b, bn));
+    if (cn) TRY(check_scalar_ptr(c, cn));
+  } else {
+    REQUIRE(a == nullptr && b == nullptr && c == nullptr, "FP8 scales must be NULL unless dtype is CODA_E4M3");
+  }
+  return CODA_OK;
+}
+
+coda_status run_gemm(coda_dtype dt, const coda::GemmProblem& p) {
+  const char* msg = "";
+  cudaError_t e;
+  switch (dt) {
+    case CODA_BF16: e = coda::launch_gemm_bf16(p, &msg); break;
+    case CODA_F32: e = coda::launch_gemm_tf32(p, &msg); break;
+    default: e = coda::launch_gemm_e4m3(p, &msg); break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, msg);
+  return CODA_OK;
+}
+
+// Programmatic dependent launch (kernel prologues overlap the previous
+// kernel's tail) is on unless CODA_NO_PDL is set in the environment.
+bool use_pdl() {
+  static const bool on = getenv("CODA_NO_PDL") == nullptr;
+  return on;
+}
+
+coda_status zero_scalar(float* p, cudaStream_t s) {
+  if (p == nullptr) return CODA_OK;
+  cudaError_t e = cudaMemsetAsync(p, 0, sizeof(float), s);
+  return e == cudaSuccess ? CODA_OK : cuda_fail(e, "cudaMemsetAsync(amax)");
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ host helpers ----
+namespace coda {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+CUresult encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+cudaError_t launch_ex(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, kernel, args);
+}
+
+}  // namespace coda
+
+// ------------------------------------------------------------------- ABI ----
+extern "C" {
+
+int coda_version(void) { return 100; }
+
+const char* coda_status_string(coda_status s) {
+  switch (s) {
+    case CODA_OK: return "CODA_OK";
+    case CODA_ERR_INVALID_ARG: return "CODA_ERR_INVALID_ARG";
+    case CODA_ERR_UNSUPPORTED: return "CODA_ERR_UNSUPPORTED";
+    case CODA_ERR_CUDA: return "CODA_ERR_CUDA";
+    case CODA_ERR_TIMEOUT: return "CODA_ERR_TIMEOUT";
+  }
+  return "unknown coda_status";
+}
+
+const char* coda_last_error(void) { return g_msg; }
+
+int64_t coda_partial_cols(int64_t N) {
+  if (N <= 0) return -1;
+  return (N + coda::kPartialCols - 1) / coda::kPartialCols;
+}
+
+coda_status coda_fold_gamma(const void* Wt, const float* gamma, void* Wt_out, int64_t N_out, int64_t K,
+                            coda_dtype dtype, cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(dtype == CODA_F32 || dtype == CODA_BF16, "coda_fold_gamma: dtype must be CODA_F32 or CODA_BF16");
+  REQUIRE(N_out >= 0 && K > 0 && N_out < INT32_MAX && K < INT32_MAX, "coda_fold_gamma: bad shape");
+  REQUIRE((K * elem_bytes(dtype)) % 16 == 0, "coda_fold_gamma: K must give 16-byte rows");
+  if (N_out == 0) return CODA_OK;
+  TRY(check_ptr(Wt, "Wt"));
+  TRY(check_ptr(gamma, "gamma"));
+  TRY(check_ptr(Wt_out, "Wt_out"));
+  const int64_t wb = N_out * K * elem_bytes(dtype);
+  const Range outs[] = {rng("Wt_out", Wt_out, wb)};
+  const Range ins[] = {rng("Wt", Wt, wb), rng("gamma", gamma, K * 4)};
+  TRY(check_overlaps(outs, 1, ins, 2));
+  cudaError_t e = coda::launch_fold_gamma(Wt, gamma, Wt_out, N_out, K, dtype == CODA_F32, stream);
+  return e == cudaSuccess ? CODA_OK : cuda_fail(e, "coda_fold_gamma launch");
+}
+
+coda_status coda_gemm_residual_partial_rms(const void* X, const void* W1t, const void* R, void* H, float* P,
+                                           int64_t M, int64_t N, int64_t K, coda_dtype dtype,
+                                           const float* scale_x, const float* scale_w, float* amax_h,
+                                           cudaStream_t stream) {
+  g_msg[0] = 0;
+  TRY(check_gemm_dims(M, N, K, dtype, "N"));
+  TRY(check_scales(dtype, scale_x, "scale_x", scale_w, "scale_w"));
+  if (amax_h) TRY(check_scalar_ptr(amax_h, "amax_h"));
+  if (M == 0) return zero_scalar(amax_h, stream);
+  TRY(check_ptr(X, "X"));
+  TRY(check_ptr(W1t, "W1t"));
+  TRY(check_ptr(R, "R"));
+  TRY(check_ptr(H, "H"));
+  TRY(check_ptr(P, "P"));
+  const int64_t T = coda_partial_cols(N);
+  const int ob = out_bytes(dtype), ib = elem_bytes(dtype);
+  const Range outs[] = {rng("H", H, M * N * ob), rng("P", P, M * T * 4), rng("amax_h", amax_h, amax_h ? 4 : 0)};
+  const Range ins[] = {rng("X", X, M * K * ib), rng("W1t", W1t, N * K * ib), rng("R", R, M * N * ob),
+                       rng("scale_x", scale_x, scale_x ? 4 : 0), rng("scale_w", scale_w, scale_w ? 4 : 0)};
+  TRY(check_overlaps(outs, 3, ins, 5));
+  TRY(zero_scalar(amax_h, stream));
+  coda::GemmProblem p = {};
+  p.epi = coda::kEpiResidualPartialRms;
+  p.A = X;
+  p.B = W1t;
+  p.R = R;
+  p.D = H;
+  p.M = static_cast<int>(M);
+  p.N_out = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.ep.P = P;
+  p.ep.T = static_cast<int>(T);
+  p.ep.scale_a = scale_x;
+  p.ep.scale_b = scale_w;
+  p.ep.amax_out = amax_h;
+  p.stream = stream;
+  p.pdl = use_pdl();
+  return run_gemm(dtype, p);
+}
+
+coda_status coda_rms_reduce(const float* P, int64_t M, int64_t N, float eps, float* r, cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(M >= 0 && M < INT32_MAX, "coda_rms_reduce: M out of range");
+  REQUIRE(N > 0 && N < INT32_MAX, "coda_rms_reduce: N out of range");
+  REQUIRE(std::isfinite(eps) && eps >= 0.0f, "coda_rms_reduce: eps must be finite and >= 0");
+  if (M == 0) return CODA_OK;
+  TRY(check_ptr(P, "P"));
+  TRY(check_ptr(r, "r"));
+  const int64_t T = coda_partial_cols(N);
+  const Range outs[] = {rng("r", r, M * 4)};
+  const Range ins[] = {rng("P", P, M * T * 4)};
+  TRY(check_overlaps(outs, 1, ins, 1));
+  cudaError_t e = coda::launch_rms_reduce(P, M, static_cast<int>(T), N, eps, r, stream, use_pdl());
+  return e == cudaSuccess ? CODA_OK : cuda_fail(e, "coda_rms_reduce launch");
+}
+
+coda_status coda_gemm_rowscale(const void* H, const void* W2t, const float* r, void* Z, int64_t M, int64_t N2,
+                               int64_t K, coda_dtype dtype, const float* scale_h, const float* scale_w,
+                               cudaStream_t stream) {
+  g_msg[0] = 0;
+  TRY(check_gemm_dims(M, N2, K, dtype, "N2"));
+  TRY(check_scales(dtype, scale_h, "scale_h", scale_w, "scale_w"));
+  if (M == 0) return CODA_OK;
+  TRY(check_ptr(H, "H"));
+  TRY(check_ptr(W2t, "W2t"));
+  TRY(check_ptr(r, "r"));
+  TRY(check_ptr(Z, "Z"));
+  const int ob = out_bytes(dtype), ib = elem_bytes(dtype);
+  const Range outs[] = {rng("Z", Z, M * N2 * ob)};
+  const Range ins[] = {rng("H", H, M * K * ib), rng("W2t", W2t, N2 * K * ib), rng("r", r, M * 4),
+                       rng("scale_h", scale_h, scale_h ? 4 : 0), rng("scale_w", scale_w, scale_w ? 4 : 0)};
+  TRY(check_overlaps(outs, 1, ins, 5));
+  coda::GemmProblem p = {};
+  p.epi = coda::kEpiRowScale;
+  p.A = H;
+  p.B = W2t;
+  p.D = Z;
+  p.M = static_cast<int>(M);
+  p.N_out = static_cast<int>(N2);
+  p.K = static_cast<int>(K);
+  p.ep.r = r;
+  p.ep.scale_a = scale_h;
+  p.ep.scale_b = scale_w;
+  p.stream = stream;
+  p.pdl = use_pdl();
+  return run_gemm(dtype, p);
+}
+
+coda_status coda_gemm_swiglu(const void* H, const void* Wgt, const void* Wut, const float* r, void* Act, int64_t M,
+                             int64_t I, int64_t K, coda_dtype dtype, const float* scale_h, const float* scale_wg,
+                             const float* scale_wu, float* amax_act, cudaStream_t stream) {
+  g_msg[0] = 0;
+  TRY(check_gemm_dims(M, I, K, dtype, "I"));
+  TRY(check_scales(dtype, scale_h, "scale_h", scale_wg, "scale_wg", scale_wu, "scale_wu"));
+  if (amax_act) TRY(check_scalar_ptr(amax_act, "amax_act"));
+  if (M == 0) return zero_scalar(amax_act, stream);
+  TRY(check_ptr(H, "H"));
+  TRY(check_ptr(Wgt, "Wgt"));
+  TRY(check_ptr(Wut, "Wut"));
+  if (r) TRY(check_scalar_ptr(r, "r"));
+  TRY(check_ptr(Act, "Act"));
+  const int ob = out_bytes(dtype), ib = elem_bytes(dtype);
+  const Range outs[] = {rng("Act", Act, M * I * ob), rng("amax_act", amax_act, amax_act ? 4 : 0)};
+  const Range ins[] = {rng("H", H, M * K * ib),
+                       rng("Wgt", Wgt, I * K * ib),
+                       rng("Wut", Wut, I * K * ib),
+                       rng("r", r, r ? M * 4 : 0),
+                       rng("scale_h", scale_h, scale_h ? 4 : 0),
+                       rng("scale_wg", scale_wg, scale_wg ? 4 : 0),
+                       rng("scale_wu", scale_wu, scale_wu ? 4 : 0)};
+  TRY(check_overlaps(outs, 2, ins, 7));
+  TRY(zero_scalar(amax_act, stream));
+  coda::GemmProblem p = {};
+  p.epi = coda::kEpiSwiGLU;
+  p.A = H;
+  p.B = Wgt;
+  p.B2 = Wut;
+  p.D = Act;
+  p.M = static_cast<int>(M);
+  p.N_out = static_cast<int>(I);
+  p.K = static_cast<int>(K);
+  p.ep.r = r;
+  p.ep.scale_a = scale_h;
+  p.ep.scale_b = scale_wg;
+  p.ep.scale_b2 = scale_wu;
+  p.ep.amax_out = amax_act;
+  p.stream = stream;
+  p.pdl = use_pdl();
+  return run_gemm(dtype, p);
+}
+
+coda_status coda_amax(const void* x, int64_t n, coda_dtype dtype, float* amax, cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(dtype == CODA_F32 || dtype == CODA_BF16, "coda_amax: dtype must be CODA_F32 or CODA_BF16");
+  REQUIRE(n >= 0, "coda_amax: n < 0");
+  TRY(check_scalar_ptr(amax, "amax"));
+  TRY(zero_scalar(amax, stream));
+  if (n == 0) return CODA_OK;
+  TRY(check_ptr(x, "x"));
+  const Range outs[] = {rng("amax", amax, 4)};
+  const Range ins[] = {rng("x", x, n * elem_bytes(dtype))};
+  TRY(check_overlaps(outs, 1, ins, 1));
+  cudaError_t e = coda::launch_amax(x, n, dtype == CODA_F32, amax, stream);
+  return e == cudaSuccess ? CODA_OK : cuda_fail(e, "coda_amax launch");
+}
+
+coda_status coda_quantize_e4m3(const void* x, int64_t n, coda_dtype dtype, const float* amax, uint8_t* q,
+                               float* scale, cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(dtype == CODA_F32 || dtype == CODA_BF16, "coda_quantize_e4m3: dtype must be CODA_F32 or CODA_BF16");
+  REQUIRE(n >= 0, "coda_quantize_e4m3: n < 0");
+  TRY(check_scalar_ptr(amax, "amax"));
+  TRY(check_scalar_ptr(scale, "scale"));
+  if (n > 0) {
+    TRY(check_ptr(x, "x"));
+    TRY(check_ptr(q, "q"));
+  }
+  const Range outs[] = {rng("q", q, n), rng("scale", scale, 4)};
+  const Range ins[] = {rng("x", x, n * elem_bytes(dtype)), rng("amax", amax, 4)};
+  TRY(check_overlaps(outs, 2, ins, 2));
+  cudaError_t e = coda::launch_quantize_e4m3(x, n, dtype == CODA_F32, amax, q, scale, stream);
+  return e == cudaSuccess ? CODA_OK : cuda_fail(e, "coda_quantize_e4m3 launch");
+}
+
+coda_status coda_get_device_status(void) {
+  g_msg[0] = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  const unsigned s = coda::read_clear_status_bf16() | coda::read_clear_status_tf32() |
+                     coda::read_clear_status_e4m3() | coda::read_clear_status_aux();
+  if (s == ~0u) return fail(CODA_ERR_CUDA, "could not read the device status word");
+  if (s & 1u) return fail(CODA_ERR_TIMEOUT, "a kernel gave up on a bounded wait (timeout)");
+  return CODA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Internal interface between the C ABI (coda_abi.cu) and the kernel
+// translation units.  Host and device code both see these definitions.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace coda {
+
+// Epilogue programs of the persistent GEMM (see gemm_epilogue.cuh).
+enum Epilogue { kEpiResidualPartialRms = 0, kEpiRowScale = 1, kEpiSwiGLU = 2 };
+
+// Width, in output columns, of one partial sum-of-squares group written by the
+// residual epilogue: P has ceil(N / kPartialCols) columns.
+constexpr int kPartialCols = 128;
+
+// Arguments of the fused epilogue programs (all device pointers).
+struct EpiParams {
+  const float* r;         // row scale [M]: required by the row-scale program, nullable (= 1) for SwiGLU
+  float* P;               // residual program: partial sums of squares [M, T]
+  int T;                  // columns of P
+  const float* scale_a;   // E4M3 operands: dequantisation scale of A, else null
+  const float* scale_b;   // ... of B (SwiGLU: of the gate weight)
+  const float* scale_b2;  // SwiGLU: of the up weight
+  float* amax_out;        // nullable: max |stored output|, combined with atomicMax (caller zeroes it)
+};
+
+struct GemmProblem {
+  int epi;                 // Epilogue
+  const void* A;           // [M, K] K-major activations
+  const void* B;           // [N_out, K] K-major weight (W^T); SwiGLU: gate weight [I, K]
+  const void* B2;          // SwiGLU: up weight [I, K]; else null
+  const void* R;           // residual program: [M, N_out] residual; else null
+  void* D;                 // [M, N_out] output
+  int M, N_out, K;
+  EpiParams ep;
+  cudaStream_t stream;
+  bool pdl;                // launch with programmatic stream serialisation
+};
+
+// One launcher per operand kind; each lives in its own translation unit so
+// the three compile in parallel.  They return cudaSuccess or the CUDA error
+// of the tensor-map encode / launch, with a message in *msg.
+cudaError_t launch_gemm_bf16(const GemmProblem& p, const char** msg);
+cudaError_t launch_gemm_tf32(const GemmProblem& p, const char** msg);
+cudaError_t launch_gemm_e4m3(const GemmProblem& p, const char** msg);
+unsigned read_clear_status_bf16();
+unsigned read_clear_status_tf32();
+unsigned read_clear_status_e4m3();
+
+// Element-wise and reduction kernels (coda_aux.cu).
+cudaError_t launch_rms_reduce(const float* P, int64_t M, int T, int64_t N, float eps, float* r,
+                              cudaStream_t s, bool pdl);
+cudaError_t launch_fold_gamma(const void* Wt, const float* gamma, void* Wt_out, int64_t N_out, int64_t K,
+                              bool f32, cudaStream_t s);
+cudaError_t launch_amax(const void* x, int64_t n, bool f32, float* amax, cudaStream_t s);
+cudaError_t launch_quantize_e4m3(const void* x, int64_t n, bool f32, const float* amax, uint8_t* q,
+                                 float* scale, cudaStream_t s);
+unsigned read_clear_status_aux();
+
+// Host helpers (coda_abi.cu).
+int device_sm_count();
+// 2-D row-major tensor map with 128-byte swizzle: `inner` contiguous
+// elements per row, `outer` rows, rows `row_bytes` apart; box of
+// box_inner x box_outer elements.
+CUresult encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// Launch `kernel` with the given shape, optionally with programmatic stream
+// serialisation (PDL), so its prologue overlaps the previous kernel's tail.
+cudaError_t launch_ex(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      void** args);
+
+}  // namespace coda

@@ -1,0 +1,522 @@
+// Persistent, warp-specialised tcgen05 GEMM with fused epilogue programs.
+//
+// D[M, N_out] = epilogue(A[M, K] . B[N_out, K]^T), both operands K-major
+// (activations [M, K] and weights W^T [N_out, K], row-major), TMA-loaded with
+// 128-byte swizzle so every k-block row of a tile is exactly 128 bytes.
+//
+// One CTA per SM walks 128-row output tiles.  Roles (warps):
+//   0      TMA producer: A and B k-blocks into a STAGES-deep shared ring
+//   1      TMEM owner + MMA issuer (one thread): tcgen05.mma into one of two
+//          256-column TMEM accumulators, so the epilogue of tile i overlaps
+//          the mainloop of tile i+1
+//   2..5   epilogue: tcgen05.ld (one accumulator row per thread) -> fused
+//          program -> 128B-swizzled shared slot -> TMA store, one 128-byte
+//          wide column box at a time
+//   6      residual program only: TMA loads of R boxes into the slot ring, so
+//          the residual add reads R from shared memory and writes h in place
+//
+// Epilogue programs.  The CODA write-ups ("CODA: the treasure hidden in the
+// epilogue") apply the memory-bound neighbours of a GEMM while its product is
+// still on chip:
+//   kEpiResidualPartialRms  h = R + acc ; P[row, g] = sum of h^2 over the
+//                           128-column group g of the row (of the stored,
+//                           rounded h).  GEMM1 of GEMM -> add -> RMSNorm -> GEMM.
+//   kEpiRowScale            Z = r_row * acc: RMSNorm's row scale moved past
+//                           the second GEMM (gamma is folded into its weight).
+//   kEpiSwiGLU              act = silu(r g) * (r u): the gate and up
+//                           accumulators of the same 128 output columns share
+//                           one N=256 MMA (B tile = 128 gate rows ++ 128 up rows).
+// E4M3 operands: acc is multiplied by the per-tensor scales of A and B first.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "coda_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace coda {
+
+// Per-translation-unit device status word (timeouts), read back and cleared
+// by the TU's read_clear_status_* function.
+namespace {
+__device__ unsigned g_status;
+}
+
+template <int KIND, int EPI, int STAGES_, int NSLOTS_>
+struct GemmCfg {
+  static constexpr int kKind = KIND;
+  static constexpr int kEpi = EPI;
+  static constexpr int BM = 128;
+  static constexpr int BN = 256;  // MMA N (SwiGLU: 128 gate + 128 up)
+  static constexpr int STAGES = STAGES_;
+  static constexpr int NSLOTS = NSLOTS_;
+  static constexpr int ELEM = KIND == kKindBF16 ? 2 : (KIND == kKindTF32 ? 4 : 1);
+  static constexpr int BK = 128 / ELEM;     // elements per k-block (one 128-byte swizzle row)
+  static constexpr int UMMA_K = 32 / ELEM;  // K of one tcgen05.mma (32 bytes)
+  static constexpr int K_STEPS = BK / UMMA_K;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int B_ROWS_PER_LOAD = EPI == kEpiSwiGLU ? BN / 2 : BN;
+  static constexpr int OUT_COLS = EPI == kEpiSwiGLU ? BN / 2 : BN;  // output columns per tile
+  static constexpr int OUT_ELEM = KIND == kKindTF32 ? 4 : 2;         // fp32 out for tf32, else bf16
+  static constexpr int BOX_COLS = 128 / OUT_ELEM;                    // output columns per 128-byte box
+  static constexpr int NUM_BOXES = OUT_COLS / BOX_COLS;
+  static constexpr int NC32 = BOX_COLS / 32;  // 32-column TMEM loads per box (per operand half)
+  static constexpr int CHUNK_COLS = 16 / OUT_ELEM;  // columns per 16-byte chunk of a box row
+  static constexpr int SLOT_BYTES = BM * 128;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int NUM_EPI_THREADS = 128;
+  static constexpr int NUM_THREADS = EPI == kEpiResidualPartialRms ? 224 : 192;
+  static constexpr int GROUP_M = 16;  // tile raster: GROUP_M M-tiles share each B panel in flight
+  // shared memory: [A stages][B stages][slots][barriers][tmem slot, abort flag]
+  static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_SLOTS = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BARS = OFF_SLOTS + NSLOTS * SLOT_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * NSLOTS + 1;
+  static constexpr int SMEM_BYTES = OFF_BARS + NUM_BARS * 8 + 16 + 1024;  // + slack for 1 KB alignment
+  static_assert(TMEM_COLS == 512, "two 256-column accumulators");
+  static_assert(OUT_COLS % BOX_COLS == 0 && BOX_COLS % 32 == 0, "box tiling");
+  static_assert(kPartialCols % BOX_COLS == 0 && OUT_COLS % kPartialCols == 0, "partial groups");
+  static_assert(NSLOTS >= 2, "slot ring");
+  static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory");
+  static constexpr uint32_t FMT = KIND == kKindBF16 ? 1u : (KIND == kKindTF32 ? 2u : 0u);
+  static constexpr uint32_t IDESC = make_idesc(FMT, FMT, BM, BN);
+};
+
+struct TileCoord {
+  int m, n;
+};
+
+// Grouped raster: consecutive tile indices walk GROUP_M M-tiles down one
+// column of output tiles before moving right, so the CTAs in flight share a
+// few A and B panels in L2.
+template <int GROUP_M>
+__device__ __forceinline__ TileCoord tile_coord(int t, int m_tiles, int n_tiles) {
+  const int per_group = GROUP_M * n_tiles;
+  const int g = t / per_group;
+  const int first_m = g * GROUP_M;
+  const int gm = min(GROUP_M, m_tiles - first_m);
+  const int local = t - g * per_group;
+  return {first_m + local % gm, local / gm};
+}
+
+// silu(x) = x * sigmoid(x) = x / (1 + e^-x); for x -> -inf the quotient
+// goes to -0, for x -> +inf to x.
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Byte offset of 16-byte chunk `c` (0..7) of row `row` inside one 128B-swizzled
+// box of 128 rows x 128 B: the chunk index is XORed with the row's position in
+// its 8-row atom, as TMA lays it out.
+__device__ __forceinline__ uint32_t swz(int row, int c) {
+  return static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+// Last-issued round of each ring stage, for draining in-flight TMA loads:
+// stage s received loads in rounds 0..(issued-1-s)/N.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int n_stages, uint32_t issued, volatile int* abort_flag) {
+  for (int s = 0; s < n_stages; ++s) {
+    if (issued > static_cast<uint32_t>(s)) {
+      const uint32_t round = (issued - 1u - static_cast<uint32_t>(s)) / static_cast<uint32_t>(n_stages);
+      (void)mbar_wait(&full[s], round & 1u, abort_flag, &g_status, false);
+    }
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NUM_THREADS, 1)
+    gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmR,
+                         const __grid_constant__ CUtensorMap tmD, int M, int N_out, int K, EpiParams ep) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::OFF_B;
+  uint8_t* slots = smem + C::OFF_SLOTS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+  uint64_t* full = bars;
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* r_full = acc_empty + 2;
+  uint64_t* r_empty = r_full + C::NSLOTS;
+  uint64_t* mma_drain = r_empty + C::NSLOTS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = (M + C::BM - 1) / C::BM;
+  const int n_tiles = (N_out + C::OUT_COLS - 1) / C::OUT_COLS;
+  const int num_tiles = m_tiles * n_tiles;
+  const int num_kb = (K + C::BK - 1) / C::BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], C::NUM_EPI_THREADS / 32);
+    }
+    for (int s = 0; s < C::NSLOTS; ++s) {
+      mbar_init(&r_full[s], 1);
+      mbar_init(&r_empty[s], 1);
+    }
+    mbar_init(mma_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if constexpr (C::kEpi == kEpiSwiGLU) tma_prefetch_desc(&tmB2);
+    if constexpr (C::kEpi == kEpiResidualPartialRms) tma_prefetch_desc(&tmR);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Everything above overlapped the previous kernel's tail; from here on we
+  // read and write global memory that it may own.
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer ----
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const TileCoord tc = tile_coord<C::GROUP_M>(t, m_tiles, n_tiles);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          const int kx = kb * C::BK;
+          uint8_t* b = sB + stage * C::B_BYTES;
+          tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kx, tc.m * C::BM, pol);
+          tma_load_2d(b, &tmB, &full[stage], kx, tc.n * C::B_ROWS_PER_LOAD, pol);
+          if constexpr (C::kEpi == kEpiSwiGLU)
+            tma_load_2d(b + C::B_ROWS_PER_LOAD * 128, &tmB2, &full[stage], kx, tc.n * C::B_ROWS_PER_LOAD, pol);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every load issued must land before the CTA may exit
+      drain_ring(full, C::STAGES, issued, abort_flag);
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer ----
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!mbar_wait(&acc_empty[buf], use ^ 1u, abort_flag, &g_status)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * C::BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, &g_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::A_BYTES));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+          for (int k = 0; k < C::K_STEPS; ++k) {
+            // 32 bytes further along K inside the swizzle atom = +2 in the
+            // descriptor's 16-byte address units
+            tc_mma<C::kKind>(d_tmem, adesc + 2u * k, bdesc + 2u * k, C::IDESC, (kb | k) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit(&acc_full[buf]);
+      }
+      // every MMA issued must complete before TMEM is released
+      tc_commit(mma_drain);
+      (void)mbar_wait(mma_drain, 0, abort_flag, &g_status, false);
+    }
+  } else if (warp == 6) {
+    // ----------------------------------------- residual loader (R boxes) ----
+    if constexpr (C::kEpi == kEpiResidualPartialRms) {
+      if (lane == 0) {
+        const uint64_t pol = l2_policy_evict_first();
+        int slot = 0;
+        uint32_t phase = 0, issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+          const TileCoord tc = tile_coord<C::GROUP_M>(t, m_tiles, n_tiles);
+          for (int b = 0; b < C::NUM_BOXES; ++b) {
+            const int col0 = tc.n * C::OUT_COLS + b * C::BOX_COLS;
+            if (col0 >= N_out) break;
+            if (!mbar_wait(&r_empty[slot], phase ^ 1u, abort_flag, &g_status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&r_full[slot], C::SLOT_BYTES);
+            tma_load_2d(slots + slot * C::SLOT_BYTES, &tmR, &r_full[slot], col0, tc.m * C::BM, pol);
+            ++issued;
+            if (++slot == C::NSLOTS) {
+              slot = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        drain_ring(r_full, C::NSLOTS, issued, abort_flag);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue ----
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    const bool leader = (warp == 2 && lane == 0);
+    float sab = 1.0f, sab2 = 1.0f;
+    if constexpr (C::kKind == kKindE4M3) {
+      sab = *ep.scale_a * *ep.scale_b;
+      if constexpr (C::kEpi == kEpiSwiGLU) sab2 = *ep.scale_a * *ep.scale_b2;
+    }
+    float amax = 0.0f;
+    int slot = 0;
+    uint32_t sphase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+      const TileCoord tc = tile_coord<C::GROUP_M>(t, m_tiles, n_tiles);
+      const int buf = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+      // one decision for all 128 threads, so no thread is left at a barrier
+      if (!named_bar_and(1, C::NUM_EPI_THREADS, mbar_wait(&acc_full[buf], use, abort_flag, &g_status))) break;
+      tc_fence_after_sync();
+      const int row = tc.m * C::BM + row_in_tile;
+      float rs = 1.0f;
+      if constexpr (C::kEpi != kEpiResidualPartialRms) {
+        if (ep.r != nullptr) rs = row < M ? ep.r[row] : 0.0f;
+      }
+      const float sg = rs * sab, su = rs * sab2;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::BN);
+      float ss = 0.0f;
+#pragma unroll 1
+      for (int b = 0; b < C::NUM_BOXES; ++b) {
+        const int col0 = tc.n * C::OUT_COLS + b * C::BOX_COLS;
+        const bool valid = col0 < N_out;  // uniform over the CTA
+        if (valid) {
+          uint32_t g[C::NC32][32];
+          uint32_t u[C::kEpi == kEpiSwiGLU ? C::NC32 : 1][32];
+#pragma unroll
+          for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + b * C::BOX_COLS + 32 * i, g[i]);
+          if constexpr (C::kEpi == kEpiSwiGLU) {
+#pragma unroll
+            for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + C::BN / 2 + b * C::BOX_COLS + 32 * i, u[i]);
+          }
+          tmem_wait_ld(g[0]);
+#pragma unroll
+          for (int i = 1; i < C::NC32; ++i) tmem_touch(g[i]);
+          if constexpr (C::kEpi == kEpiSwiGLU) {
+#pragma unroll
+            for (int i = 0; i < C::NC32; ++i) tmem_touch(u[i]);
+          }
+          if (b == C::NUM_BOXES - 1 || tc.n * C::OUT_COLS + (b + 1) * C::BOX_COLS >= N_out) {
+            // last TMEM read of this tile: hand the accumulator back to the MMA warp
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          }
+          bool got = true;
+          if constexpr (C::kEpi == kEpiResidualPartialRms) got = mbar_wait(&r_full[slot], sphase, abort_flag, &g_status);
+          uint8_t* sp = slots + slot * C::SLOT_BYTES;
+#pragma unroll
+          for (int c = 0; c < (got ? 8 : 0); ++c) {
+            float o[C::CHUNK_COLS];
+#pragma unroll
+            for (int e = 0; e < C::CHUNK_COLS; ++e) {
+              const int j = c * C::CHUNK_COLS + e;
+              const float a = __uint_as_float(g[j >> 5][j & 31]);
+              if constexpr (C::kEpi == kEpiSwiGLU) {
+                const float uu = __uint_as_float(u[j >> 5][j & 31]);
+                o[e] = silu_f(a * sg) * (uu * su);
+              } else {
+                o[e] = a * sg;
+              }
+            }
+            void* p = sp + swz(row_in_tile, c);
+            if constexpr (C::OUT_ELEM == 2) {
+              uint32_t w[4];
+              if constexpr (C::kEpi == kEpiResidualPartialRms) {
+                const uint4 rv = *reinterpret_cast<const uint4*>(p);
+                const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(bf16_lo(rw[e]) + o[2 * e], bf16_hi(rw[e]) + o[2 * e + 1]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(o[2 * e], o[2 * e + 1]);
+              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // statistics of the values actually stored (bf16-rounded)
+                const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
+                if constexpr (C::kEpi == kEpiResidualPartialRms) ss += lo * lo + hi * hi;
+                if (ep.amax_out) amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+              }
+              *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+              float4 v = make_float4(o[0], o[1], o[2], o[3]);
+              if constexpr (C::kEpi == kEpiResidualPartialRms) {
+                const float4 rv = *reinterpret_cast<const float4*>(p);
+                v.x += rv.x;
+                v.y += rv.y;
+                v.z += rv.z;
+                v.w += rv.w;
+                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+              }
+              if (ep.amax_out) amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+              *reinterpret_cast<float4*>(p) = v;
+            }
+          }
+          if constexpr (C::kEpi == kEpiResidualPartialRms) {
+            const int gcol = col0 + C::BOX_COLS;  // end column of this box
+            if (gcol % kPartialCols == 0 || gcol >= N_out) {
+              const int pc = col0 / kPartialCols;
+              if (row < M) ep.P[static_cast<int64_t>(row) * ep.T + pc] = ss;
+              ss = 0.0f;
+            }
+          }
+          // shared slot -> global
+          fence_proxy_async_smem();
+          if (!named_bar_and(1, C::NUM_EPI_THREADS, got)) {
+            ok = false;
+            break;
+          }
+          if (leader) {
+            tma_store_2d(&tmD, sp, col0, tc.m * C::BM);
+            tma_store_commit();
+            tma_store_wait_read_all();  // slot readable again before anyone rewrites it
+            if constexpr (C::kEpi == kEpiResidualPartialRms) mbar_arrive(&r_empty[slot]);
+          }
+          if (++slot == C::NSLOTS) {
+            slot = 0;
+            sphase ^= 1u;
+          }
+        }
+      }
+    }
+    if (ep.amax_out) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      // non-negative floats order like their bit patterns
+      if (lane == 0) atomicMax(reinterpret_cast<int*>(ep.amax_out), __float_as_int(amax));
+    }
+    if (leader) tma_store_wait_all();
+  }
+
+  // --------------------------------------------------------------- teardown ----
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host ----
+
+template <class C>
+cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
+  CUtensorMapDataType in_dt = C::kKind == kKindBF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                              : C::kKind == kKindTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUtensorMapDataType out_dt = C::OUT_ELEM == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap tmA, tmB, tmB2, tmR, tmD;
+  const uint64_t kbytes = static_cast<uint64_t>(p.K) * C::ELEM;
+  const uint64_t obytes = static_cast<uint64_t>(p.N_out) * C::OUT_ELEM;
+  CUresult e = encode_tmap_2d(&tmA, in_dt, p.A, p.K, p.M, kbytes, C::BK, C::BM);
+  if (e == CUDA_SUCCESS) e = encode_tmap_2d(&tmB, in_dt, p.B, p.K, p.N_out, kbytes, C::BK, C::B_ROWS_PER_LOAD);
+  if (e == CUDA_SUCCESS)
+    e = encode_tmap_2d(&tmB2, in_dt, C::kEpi == kEpiSwiGLU ? p.B2 : p.B, p.K, p.N_out, kbytes, C::BK,
+                       C::B_ROWS_PER_LOAD);
+  if (e == CUDA_SUCCESS)
+    e = encode_tmap_2d(&tmR, out_dt, C::kEpi == kEpiResidualPartialRms ? p.R : p.D, p.N_out, p.M, obytes,
+                       C::BOX_COLS, C::BM);
+  if (e == CUDA_SUCCESS) e = encode_tmap_2d(&tmD, out_dt, p.D, p.N_out, p.M, obytes, C::BOX_COLS, C::BM);
+  if (e != CUDA_SUCCESS) {
+    *msg = "cuTensorMapEncodeTiled rejected an operand (pointer, stride or extent)";
+    return cudaErrorInvalidValue;
+  }
+  auto kernel = gemm_epilogue_kernel<C>;
+  static int configured_mask = 0;  // one bit per device ordinal < 31
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return ce;
+  if (dev >= 31 || !(configured_mask & (1 << dev))) {
+    ce = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (ce != cudaSuccess) {
+      *msg = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
+      return ce;
+    }
+    if (dev < 31) configured_mask |= 1 << dev;
+  }
+  const int m_tiles = (p.M + C::BM - 1) / C::BM;
+  const int n_tiles = (p.N_out + C::OUT_COLS - 1) / C::OUT_COLS;
+  const int num_tiles = m_tiles * n_tiles;
+  const int grid = num_tiles < device_sm_count() ? num_tiles : device_sm_count();
+  int M = p.M, N = p.N_out, K = p.K;
+  EpiParams ep = p.ep;
+  void* args[] = {&tmA, &tmB, &tmB2, &tmR, &tmD, &M, &N, &K, &ep};
+  ce = launch_ex(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(C::NUM_THREADS), C::SMEM_BYTES, p.stream,
+                 p.pdl, args);
+  if (ce != cudaSuccess) *msg = "GEMM kernel launch failed";
+  return ce;
+}
+
+// Residual program: 3 mainloop stages + 4 R slots; the others: 4 stages + 2
+// output slots (both fit the 227 KB of shared memory per CTA).
+template <int KIND>
+cudaError_t launch_gemm(const GemmProblem& p, const char** msg) {
+  switch (p.epi) {
+    case kEpiResidualPartialRms:
+      return launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, 3, 4>>(p, msg);
+    case kEpiRowScale:
+      return launch_cfg<GemmCfg<KIND, kEpiRowScale, 4, 2>>(p, msg);
+    case kEpiSwiGLU:
+      return launch_cfg<GemmCfg<KIND, kEpiSwiGLU, 4, 2>>(p, msg);
+    default:
+      *msg = "unknown epilogue program";
+      return cudaErrorInvalidValue;
+  }
+}
+
+inline unsigned read_clear_status_impl() {
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return ~0u;
+  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return ~0u;
+  return v;
+}
+
+}  // namespace coda

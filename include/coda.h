@@ -1,0 +1,176 @@
+/*
+ * coda.h -- C ABI of the GB300 (sm_103a) fused GEMM-epilogue library.
+ *
+ * The library implements the forward hot path of "CODA: Rewriting Transformer
+ * Blocks as GEMM-Epilogue Programs" as the CODA news write-up describes it
+ * (KuCoin news, "CODA new research optimizes transformer training with
+ * GEMM-epilogue programming"; the same article on itsolotime.com and on
+ * KuCoin's Arabic site):
+ *
+ *   section "CODA: the treasure hidden in the epilogue":
+ *     GEMM -> residual add -> RMSNorm -> GEMM.  RMSNorm's per-row scale r is a
+ *     scalar shared by the whole row, so it commutes with the next matmul and
+ *     can be applied in the second GEMM's epilogue; the first GEMM's epilogue
+ *     then only computes local partial RMS statistics, which a very light
+ *     auxiliary reduction kernel folds into r.  SwiGLU admits the same
+ *     reparameterisation.
+ *   section "five blocks and a Lego language":
+ *     the epilogue primitives used here -- element-wise transforms (residual
+ *     add, activation), vector load (the broadcast RMSNorm weight, folded into
+ *     the next weight here) and block reduction (local RMS).
+ *
+ * The block computed by a chain of calls (row i of M tokens, hidden width N):
+ *     h    = R + X . W1                                coda_gemm_residual_partial_rms
+ *     r_i  = 1 / sqrt(mean_j h_ij^2 + eps)             coda_rms_reduce
+ *     W2'  = diag(gamma) . W2                          coda_fold_gamma (once per weight)
+ *     Z    = diag(r) . h . W2'      == RMSNorm(h).W2   coda_gemm_rowscale
+ *     act  = silu(r h Wg') * (r h Wu')                 coda_gemm_swiglu
+ * with RMSNorm(h)_ij = h_ij * r_i * gamma_j and silu(x) = x / (1 + e^-x).
+ *
+ * Conventions shared by every call
+ *   - Matrices are row-major.  Activations are [rows, K]; a weight W [K, N]
+ *     is passed as its transpose W^T [N, K] (the nn.Linear weight layout), so
+ *     both GEMM operands are K-major.
+ *   - Pointers are DEVICE pointers unless stated otherwise, 16-byte aligned.
+ *     Every row of every matrix must start on a 16-byte boundary: K and the
+ *     output width must be multiples of 4 (CODA_F32), 8 (CODA_BF16) or 16
+ *     (CODA_E4M3 operands).
+ *   - Sizes are int64_t; M may be 0 (nothing is launched), N and K must be
+ *     positive; every dimension must be below 2^31.
+ *   - Ownership: the caller owns all memory.  The library never allocates,
+ *     frees or synchronises; every call only enqueues work on `stream`
+ *     (cudaStream_t; NULL = the legacy default stream) and returns.
+ *   - Outputs must not overlap any input or each other (checked on the
+ *     address ranges; CODA_ERR_INVALID_ARG otherwise).
+ *   - Errors: argument checks run before anything is enqueued and return
+ *     CODA_ERR_INVALID_ARG (nothing written); CUDA errors from encoding or
+ *     launching return CODA_ERR_CUDA.  coda_last_error() describes the last
+ *     failure of the calling thread.  Device-side wait timeouts (a kernel
+ *     that gave up instead of hanging) are reported by coda_get_device_status().
+ *   - dtype: CODA_F32 = fp32 operands and outputs (tensor cores in tf32 with
+ *     fp32 accumulation); CODA_BF16 = bf16 operands and outputs (fp32
+ *     accumulation); CODA_E4M3 = OCP FP8 e4m3 GEMM operands, each with a
+ *     per-tensor fp32 dequantisation scale (device pointer), fp32
+ *     accumulation, bf16 residual and outputs.
+ */
+#ifndef CODA_H_
+#define CODA_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define CODA_API __attribute__((visibility("default")))
+#else
+#define CODA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CODA_OK = 0,
+  CODA_ERR_INVALID_ARG = 1,
+  CODA_ERR_UNSUPPORTED = 2,
+  CODA_ERR_CUDA = 3,
+  CODA_ERR_TIMEOUT = 4
+} coda_status;
+
+typedef enum { CODA_F32 = 0, CODA_BF16 = 1, CODA_E4M3 = 2 } coda_dtype;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+CODA_API int coda_version(void);
+
+/* Human-readable name of a status code (static string). */
+CODA_API const char* coda_status_string(coda_status s);
+
+/* Message describing the last failed call on this host thread (static,
+ * thread-local storage; "" if none). */
+CODA_API const char* coda_last_error(void);
+
+/* Number of partial-sum columns T = ceil(N / 128) that
+ * coda_gemm_residual_partial_rms writes per row for hidden width N: the
+ * caller allocates P as fp32 [M, T].  Returns -1 for N <= 0. */
+CODA_API int64_t coda_partial_cols(int64_t N);
+
+/* One-time weight transform W' = diag(gamma) . W (not on the pages as a
+ * separate step: it is where the broadcast RMSNorm weight of the "five
+ * blocks" section goes once r has been moved past the GEMM).
+ *   Wt      [N_out, K] input weight W^T (dtype CODA_F32 or CODA_BF16)
+ *   gamma   [K] fp32 RMSNorm weight of the hidden dimension K
+ *   Wt_out  [N_out, K] output W'^T, same dtype: Wt_out[n, k] = Wt[n, k] * gamma[k]
+ *           (computed in fp32, rounded to nearest-even once).  May not alias Wt.
+ * For FP8, fold in bf16 or fp32 first, then coda_amax + coda_quantize_e4m3. */
+CODA_API coda_status coda_fold_gamma(const void* Wt, const float* gamma, void* Wt_out, int64_t N_out, int64_t K,
+                            coda_dtype dtype, cudaStream_t stream);
+
+/* GEMM1 with the residual add and the partial RMS statistics in its epilogue
+ * (section "CODA: the treasure hidden in the epilogue"):
+ *   h[i, j]  = R[i, j] + sum_k X[i, k] * W1t[j, k]        (fp32 accumulate, stored
+ *                                                           rounded to the output type)
+ *   P[i, g]  = sum over j in [128 g, 128 g + 128) of h[i, j]^2   (of the stored h)
+ *   X   [M, K]   dtype operands (CODA_E4M3: e4m3 bytes)
+ *   W1t [N, K]   dtype operands
+ *   R   [M, N]   residual: fp32 for CODA_F32, else bf16
+ *   H   [M, N]   output h, same type as R.  Must not alias R.
+ *   P   [M, coda_partial_cols(N)] fp32 output
+ *   scale_x, scale_w: CODA_E4M3 only (device fp32 scalars; the product
+ *           X.W1t is multiplied by *scale_x * *scale_w); must be NULL otherwise.
+ *   amax_h: nullable device fp32 scalar; when given it receives max |h|
+ *           (overwritten, not accumulated), for quantising h to FP8 next. */
+CODA_API coda_status coda_gemm_residual_partial_rms(const void* X, const void* W1t, const void* R, void* H, float* P,
+                                           int64_t M, int64_t N, int64_t K, coda_dtype dtype,
+                                           const float* scale_x, const float* scale_w, float* amax_h,
+                                           cudaStream_t stream);
+
+/* The auxiliary reduction ("a very light auxiliary reduction kernel"):
+ *   r[i] = 1 / sqrt( (sum_g P[i, g]) / N + eps )
+ *   P [M, coda_partial_cols(N)] fp32 partials of a hidden width N; r [M] fp32.
+ *   eps >= 0 and finite. */
+CODA_API coda_status coda_rms_reduce(const float* P, int64_t M, int64_t N, float eps, float* r, cudaStream_t stream);
+
+/* GEMM2 with RMSNorm's row scale applied in its epilogue:
+ *   Z[i, n] = r[i] * sum_k H[i, k] * W2t[n, k]
+ * which equals RMSNorm(h) . W2 when W2t = (diag(gamma) W2)^T from coda_fold_gamma.
+ *   H [M, K], W2t [N2, K] dtype operands; r [M] fp32 (required);
+ *   Z [M, N2]: fp32 for CODA_F32, else bf16.
+ *   scale_h, scale_w: as for coda_gemm_residual_partial_rms. */
+CODA_API coda_status coda_gemm_rowscale(const void* H, const void* W2t, const float* r, void* Z, int64_t M, int64_t N2,
+                               int64_t K, coda_dtype dtype, const float* scale_h, const float* scale_w,
+                               cudaStream_t stream);
+
+/* Gate/up GEMM with SwiGLU (and the row scale) in its epilogue:
+ *   G = r . (H . Wgt^T),  U = r . (H . Wut^T)   (row scale applied to both
+ *   before the non-linearity),  Act[i, n] = silu(G[i, n]) * U[i, n]
+ *   H [M, K], Wgt [I, K], Wut [I, K] dtype operands; r [M] fp32 or NULL (= 1);
+ *   Act [M, I]: fp32 for CODA_F32, else bf16.
+ *   scale_h, scale_wg, scale_wu: CODA_E4M3 only, NULL otherwise.
+ *   amax_act: nullable; receives max |Act| (overwritten). */
+CODA_API coda_status coda_gemm_swiglu(const void* H, const void* Wgt, const void* Wut, const float* r, void* Act, int64_t M,
+                             int64_t I, int64_t K, coda_dtype dtype, const float* scale_h, const float* scale_wg,
+                             const float* scale_wu, float* amax_act, cudaStream_t stream);
+
+/* Per-tensor absolute maximum: *amax = max_i |x_i| over n elements of
+ * dtype CODA_F32 or CODA_BF16 (overwritten).  n may be 0 (amax = 0).
+ * The FP8 operands of the block's LLaMA-8B workload use per-tensor scales. */
+CODA_API coda_status coda_amax(const void* x, int64_t n, coda_dtype dtype, float* amax, cudaStream_t stream);
+
+/* Per-tensor FP8 quantisation with the scale s = amax / 448 (s = 1 when
+ * amax == 0): q_i = e4m3(x_i / s), rounded to nearest-even and saturated to
+ * +-448 (OCP e4m3, no infinities).  x [n] CODA_F32 or CODA_BF16; amax: device
+ * fp32 scalar from coda_amax or from a GEMM's amax output; q [n] bytes
+ * (16-byte aligned, n a multiple of 16); scale: device fp32 scalar receiving s,
+ * the dequantisation scale to pass to the GEMMs. */
+CODA_API coda_status coda_quantize_e4m3(const void* x, int64_t n, coda_dtype dtype, const float* amax, uint8_t* q,
+                               float* scale, cudaStream_t stream);
+
+/* Synchronises the current device, then reads and clears the device status
+ * word: CODA_ERR_TIMEOUT if any kernel since the last call gave up on a
+ * bounded wait, CODA_ERR_CUDA if the device reports an error, else CODA_OK. */
+CODA_API coda_status coda_get_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CODA_H_ */

@@ -1,0 +1,106 @@
+"""The C ABI on the host, with no GPU: the library loads, exports every
+symbol include/coda.h declares, and rejects bad arguments before anything
+is enqueued (fake, never-dereferenced addresses are enough for that)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_epilogue_fusion_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "coda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return g.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CODA_API\s+[\w\s\*]+?\b(coda_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("coda_gemm_residual_partial_rms", "coda_rms_reduce", "coda_gemm_rowscale", "coda_gemm_swiglu",
+              "coda_fold_gamma"):
+        assert n in names
+    assert set(names) == set(g.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+    assert lib.coda_version() >= 100
+
+
+def test_partial_cols_and_status_strings(lib):
+    assert [lib.coda_partial_cols(n) for n in (1, 128, 129, 2048, 4096, 0)] == [1, 1, 2, 16, 32, -1]
+    assert lib.coda_status_string(4) == b"CODA_ERR_TIMEOUT"
+
+
+A = 0x7F0000000000  # fake 16-byte-aligned device addresses, never dereferenced
+MB = 1 << 20
+
+
+def _rpr(lib, X=A, W=A + 64 * MB, R=A + 128 * MB, H=A + 192 * MB, P=A + 256 * MB, M=256, N=512, K=512, dt=1,
+         sx=None, sw=None, amax=None):
+    return lib.coda_gemm_residual_partial_rms(X, W, R, H, P, M, N, K, dt, sx, sw, amax, None)
+
+
+def test_rejects_null_and_misaligned(lib):
+    assert _rpr(lib, X=None) == g.CODA_ERR_INVALID_ARG
+    assert b"X is NULL" in lib.coda_last_error()
+    assert _rpr(lib, H=A + 192 * MB + 8) == g.CODA_ERR_INVALID_ARG
+    assert b"16-byte" in lib.coda_last_error()
+
+
+def test_rejects_bad_shapes(lib):
+    assert _rpr(lib, K=0) == g.CODA_ERR_INVALID_ARG
+    assert _rpr(lib, N=-4) == g.CODA_ERR_INVALID_ARG
+    assert _rpr(lib, K=12) == g.CODA_ERR_INVALID_ARG          # bf16 rows of 24 bytes
+    assert _rpr(lib, N=100) == g.CODA_ERR_INVALID_ARG         # bf16 rows of 200 bytes
+    assert _rpr(lib, K=8, dt=2, sx=A + 300 * MB, sw=A + 300 * MB + 4) == g.CODA_ERR_INVALID_ARG  # e4m3: K % 16
+    assert _rpr(lib, M=1 << 31) == g.CODA_ERR_INVALID_ARG
+    assert _rpr(lib, dt=7) == g.CODA_ERR_INVALID_ARG
+
+
+def test_rejects_overlapping_outputs(lib):
+    assert _rpr(lib, H=A + 128 * MB) == g.CODA_ERR_INVALID_ARG   # h over R
+    assert b"overlaps input R" in lib.coda_last_error()
+    assert _rpr(lib, P=A + 192 * MB + 4096) == g.CODA_ERR_INVALID_ARG  # P inside h
+    assert lib.coda_gemm_rowscale(A, A + MB, A + 2 * MB, A + 100, 16, 64, 64, 1, None, None, None) \
+        == g.CODA_ERR_INVALID_ARG
+
+
+def test_fp8_scale_rules(lib):
+    # scales are required for e4m3 and forbidden otherwise
+    assert _rpr(lib, dt=2) == g.CODA_ERR_INVALID_ARG
+    assert _rpr(lib, dt=1, sx=A + 300 * MB, sw=A + 300 * MB + 4) == g.CODA_ERR_INVALID_ARG
+
+
+def test_m_zero_enqueues_nothing(lib):
+    # no amax output: nothing to do, no CUDA call is made
+    assert _rpr(lib, M=0) == g.CODA_OK
+    assert lib.coda_rms_reduce(A, 0, 512, 1e-5, A + MB, None) == g.CODA_OK
+    assert lib.coda_gemm_rowscale(A, A + MB, A + 2 * MB, A + 3 * MB, 0, 64, 64, 1, None, None, None) == g.CODA_OK
+
+
+def test_rms_reduce_and_helpers_validate(lib):
+    assert lib.coda_rms_reduce(A, 16, 512, -1.0, A + MB, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_rms_reduce(A, 16, 512, float("nan"), A + MB, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_rms_reduce(A, 16, 512, 1e-5, A + 16, None) == g.CODA_ERR_INVALID_ARG  # r inside P
+    assert lib.coda_fold_gamma(A, A + MB, A, 16, 64, 1, None) == g.CODA_ERR_INVALID_ARG  # in place
+    assert lib.coda_fold_gamma(A, A + MB, A + 2 * MB, 16, 64, 2, None) == g.CODA_ERR_INVALID_ARG  # e4m3 fold
+    assert lib.coda_amax(A, 16, 2, A + MB, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_quantize_e4m3(A, 64, 1, None, A + MB, A + 2 * MB, None) == g.CODA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    X = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        g.coda_gemm_residual_partial_rms(X, X, X, X, X)
