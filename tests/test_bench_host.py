@@ -1,0 +1,36 @@
+"""Host-side arithmetic of bench.py (no GPU): flop and byte accounting and
+the rule that a recorded ncu traffic figure is only used for the kernel
+sources it was taken on."""
+import os
+
+import pytest
+
+import bench
+
+
+def test_flops_of_llama1b_block():
+    fl = bench.flops_swiglu_chain(8192, 2048, 2048, 8192)
+    assert fl["gemm_residual"] == 2 * 8192 * 2048 * 2048
+    assert fl["swiglu"] == 2 * 8192 * 16384 * 2048
+    assert sum(fl.values()) / 1e9 == pytest.approx(618.5, abs=0.1)
+
+
+def test_fused_moves_fewer_bytes_than_unfused():
+    fused, unfused = bench.algorithmic_bytes(8192, 2048, 2048, 8192, 16)
+    assert sum(fused.values()) / 1e6 == pytest.approx(345.0, abs=2.0)
+    assert unfused / 1e6 == pytest.approx(1015.0, abs=10.0)
+    assert unfused / sum(fused.values()) > 2.5
+
+
+def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    csrc = tmp_path / "gemm_epilogue_fusion_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("kernel v1")
+    (tmp_path / "profiles").mkdir()
+    sha = bench.kernel_source_sha()
+    (tmp_path / "profiles" / "ncu_x.md").write_text(f"source_sha: {sha}\ndram_bytes_per_launch: 1.5e8\n")
+    assert bench.recorded_traffic("x") == 1.5e8
+    (csrc / "k.cu").write_text("kernel v2")
+    assert bench.recorded_traffic("x") is None
+    assert bench.recorded_traffic("missing") is None
