@@ -66,8 +66,9 @@ int device_sm_count();
 CUresult encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 // Launch `kernel` with the given shape, optionally with programmatic stream
-// serialisation (PDL), so its prologue overlaps the previous kernel's tail.
+// serialisation (PDL), so its prologue overlaps the previous kernel's tail,
+// and in clusters of `cluster` CTAs along x.
 cudaError_t launch_ex(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                      void** args);
+                      void** args, int cluster = 1);
 
 }  // namespace coda

@@ -30,6 +30,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <cstdlib>
 
 #include "coda_internal.h"
 #include "sm103_ptx.cuh"
@@ -42,12 +43,14 @@ namespace {
 __device__ unsigned g_status;
 }
 
-template <int KIND, int EPI, int STAGES_, int NSLOTS_>
+template <int KIND, int EPI, int STAGES_, int NSLOTS_, int CG_ = 1>
 struct GemmCfg {
   static constexpr int kKind = KIND;
   static constexpr int kEpi = EPI;
-  static constexpr int BM = 128;
-  static constexpr int BN = 256;  // MMA N (SwiGLU: 128 gate + 128 up)
+  static constexpr int CG = CG_;              // CTAs per MMA (cta_group::1 or ::2)
+  static constexpr int BM = 128;              // accumulator rows per CTA
+  static constexpr int TILE_M = BM * CG;      // output rows per tile (per CTA pair)
+  static constexpr int BN = 256;              // MMA N (SwiGLU: 128 gate + 128 up)
   static constexpr int STAGES = STAGES_;
   static constexpr int NSLOTS = NSLOTS_;
   static constexpr int ELEM = KIND == kKindBF16 ? 2 : (KIND == kKindTF32 ? 4 : 1);
@@ -55,9 +58,12 @@ struct GemmCfg {
   static constexpr int UMMA_K = 32 / ELEM;  // K of one tcgen05.mma (32 bytes)
   static constexpr int K_STEPS = BK / UMMA_K;
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int B_ROWS_PER_LOAD = EPI == kEpiSwiGLU ? BN / 2 : BN;
+  static constexpr int B_ROWS = BN / CG;    // B rows held by this CTA
+  static constexpr int B_BYTES = B_ROWS * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // this CTA's bytes per stage
+  // rows of one B TMA box: SwiGLU with one CTA loads gate and up halves
+  // separately; with a pair, each CTA loads one of them whole
+  static constexpr int B_BOX_ROWS = (EPI == kEpiSwiGLU && CG == 1) ? BN / 2 : B_ROWS;
   static constexpr int OUT_COLS = EPI == kEpiSwiGLU ? BN / 2 : BN;  // output columns per tile
   static constexpr int OUT_ELEM = KIND == kKindTF32 ? 4 : 2;         // fp32 out for tf32, else bf16
   static constexpr int BOX_COLS = 128 / OUT_ELEM;                    // output columns per 128-byte box
@@ -68,20 +74,21 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int NUM_EPI_THREADS = 128;
   static constexpr int NUM_THREADS = EPI == kEpiResidualPartialRms ? 224 : 192;
-  static constexpr int GROUP_M = 16;  // tile raster: GROUP_M M-tiles share each B panel in flight
+  static constexpr int GROUP_M = 16 / CG;  // tile raster: 2048-row bands share each B panel in flight
   // shared memory: [A stages][B stages][slots][barriers][tmem slot, abort flag]
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SLOTS = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BARS = OFF_SLOTS + NSLOTS * SLOT_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * NSLOTS + 1;
   static constexpr int SMEM_BYTES = OFF_BARS + NUM_BARS * 8 + 16 + 1024;  // + slack for 1 KB alignment
+  static_assert(CG == 1 || CG == 2, "CTA group");
   static_assert(TMEM_COLS == 512, "two 256-column accumulators");
   static_assert(OUT_COLS % BOX_COLS == 0 && BOX_COLS % 32 == 0, "box tiling");
   static_assert(kPartialCols % BOX_COLS == 0 && OUT_COLS % kPartialCols == 0, "partial groups");
   static_assert(NSLOTS >= 2, "slot ring");
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory");
   static constexpr uint32_t FMT = KIND == kKindBF16 ? 1u : (KIND == kKindTF32 ? 2u : 0u);
-  static constexpr uint32_t IDESC = make_idesc(FMT, FMT, BM, BN);
+  static constexpr uint32_t IDESC = make_idesc(FMT, FMT, TILE_M, BN);
 };
 
 struct TileCoord {
@@ -119,8 +126,8 @@ __device__ __forceinline__ uint32_t swz(int row, int c) {
   return static_cast<uint32_t>(row * 128 + ((c ^ (row & 7)) << 4));
 }
 
-// Last-issued round of each ring stage, for draining in-flight TMA loads:
-// stage s received loads in rounds 0..(issued-1-s)/N.
+// Let every TMA load this thread issued into a ring land before exit: stage
+// s received loads in rounds 0..(issued-1-s)/N; wait for the last one.
 __device__ __forceinline__ void drain_ring(uint64_t* full, int n_stages, uint32_t issued, volatile int* abort_flag) {
   for (int s = 0; s < n_stages; ++s) {
     if (issued > static_cast<uint32_t>(s)) {
@@ -153,7 +160,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_tiles = (M + C::BM - 1) / C::BM;
+  // CTA pair (CG = 2): rank 0 issues the MMAs for both; each CTA loads and
+  // stores its own 128 rows and half of the B tile
+  const uint32_t cta_rank = C::CG == 2 ? cluster_ctarank() : 0u;
+  const bool mma_cta = cta_rank == 0;
+  const int unit = blockIdx.x / C::CG;     // tile-walking unit (a CTA or a CTA pair)
+  const int n_units = gridDim.x / C::CG;
+  const int m_tiles = (M + C::TILE_M - 1) / C::TILE_M;
   const int n_tiles = (N_out + C::OUT_COLS - 1) / C::OUT_COLS;
   const int num_tiles = m_tiles * n_tiles;
   const int num_kb = (K + C::BK - 1) / C::BK;
@@ -165,7 +178,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], C::NUM_EPI_THREADS / 32);
+      mbar_init(&acc_empty[b], C::CG * C::NUM_EPI_THREADS / 32);
     }
     for (int s = 0; s < C::NSLOTS; ++s) {
       mbar_init(&r_full[s], 1);
@@ -183,11 +196,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<C::CG>(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish<C::CG>();
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (C::CG == 2) cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -200,23 +214,38 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     // ------------------------------------------------------- TMA producer ----
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
+      // the stage's completion is counted on the MMA CTA's barrier
+      const uint32_t full0 = C::CG == 2 ? mapa_shared(smem_u32(full), 0) : 0u;
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = unit; t < num_tiles && ok; t += n_units) {
         const TileCoord tc = tile_coord<C::GROUP_M>(t, m_tiles, n_tiles);
+        const int a_row = tc.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
           const int kx = kb * C::BK;
+          uint8_t* a = sA + stage * C::A_BYTES;
           uint8_t* b = sB + stage * C::B_BYTES;
-          tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kx, tc.m * C::BM, pol);
-          tma_load_2d(b, &tmB, &full[stage], kx, tc.n * C::B_ROWS_PER_LOAD, pol);
-          if constexpr (C::kEpi == kEpiSwiGLU)
-            tma_load_2d(b + C::B_ROWS_PER_LOAD * 128, &tmB2, &full[stage], kx, tc.n * C::B_ROWS_PER_LOAD, pol);
+          if constexpr (C::CG == 1) {
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            tma_load_2d(a, &tmA, &full[stage], kx, a_row, pol);
+            tma_load_2d(b, &tmB, &full[stage], kx, tc.n * C::B_BOX_ROWS, pol);
+            if constexpr (C::kEpi == kEpiSwiGLU)
+              tma_load_2d(b + C::B_BOX_ROWS * 128, &tmB2, &full[stage], kx, tc.n * C::B_BOX_ROWS, pol);
+          } else {
+            // the MMA CTA expects both CTAs' bytes; the peer only issues its copies
+            if (mma_cta) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+            const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
+            tma_load_2d_pair(a, &tmA, fb, kx, a_row, pol);
+            if constexpr (C::kEpi == kEpiSwiGLU)  // rank 0: gate rows, rank 1: up rows
+              tma_load_2d_pair(b, cta_rank == 0 ? &tmB : &tmB2, fb, kx, tc.n * C::B_ROWS, pol);
+            else
+              tma_load_2d_pair(b, &tmB, fb, kx, tc.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS, pol);
+          }
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -224,17 +253,19 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           }
         }
       }
-      // every load issued must land before the CTA may exit
-      drain_ring(full, C::STAGES, issued, abort_flag);
+      // every load issued must land before the CTA may exit (for a pair, the
+      // MMA CTA's ring counts both CTAs' copies)
+      if (mma_cta) drain_ring(full, C::STAGES, issued, abort_flag);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer ----
-    if (lane == 0) {
+    if (lane == 0 && mma_cta) {
+      constexpr uint16_t kPair = C::CG == 2 ? 3 : 1;
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+      for (int t = unit; t < num_tiles && ok; t += n_units, ++it) {
         const int buf = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
         if (!mbar_wait(&acc_empty[buf], use ^ 1u, abort_flag, &g_status)) break;
@@ -252,18 +283,18 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           for (int k = 0; k < C::K_STEPS; ++k) {
             // 32 bytes further along K inside the swizzle atom = +2 in the
             // descriptor's 16-byte address units
-            tc_mma<C::kKind>(d_tmem, adesc + 2u * k, bdesc + 2u * k, C::IDESC, (kb | k) != 0);
+            tc_mma<C::kKind, C::CG>(d_tmem, adesc + 2u * k, bdesc + 2u * k, C::IDESC, (kb | k) != 0);
           }
-          tc_commit(&empty[stage]);
+          tc_commit<C::CG>(&empty[stage], kPair);  // both CTAs' stage is free again
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) tc_commit(&acc_full[buf]);
+        if (ok) tc_commit<C::CG>(&acc_full[buf], kPair);
       }
       // every MMA issued must complete before TMEM is released
-      tc_commit(mma_drain);
+      tc_commit<C::CG>(mma_drain, 1);
       (void)mbar_wait(mma_drain, 0, abort_flag, &g_status, false);
     }
   } else if (warp == 6) {
@@ -274,8 +305,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         int slot = 0;
         uint32_t phase = 0, issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int t = unit; t < num_tiles && ok; t += n_units) {
           const TileCoord tc = tile_coord<C::GROUP_M>(t, m_tiles, n_tiles);
+          const int row0 = tc.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
+          if (row0 >= M) continue;  // this CTA's half of the tile is empty
           for (int b = 0; b < C::NUM_BOXES; ++b) {
             const int col0 = tc.n * C::OUT_COLS + b * C::BOX_COLS;
             if (col0 >= N_out) break;
@@ -284,7 +317,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               break;
             }
             mbar_arrive_expect_tx(&r_full[slot], C::SLOT_BYTES);
-            tma_load_2d(slots + slot * C::SLOT_BYTES, &tmR, &r_full[slot], col0, tc.m * C::BM, pol);
+            tma_load_2d(slots + slot * C::SLOT_BYTES, &tmR, &r_full[slot], col0, row0, pol);
             ++issued;
             if (++slot == C::NSLOTS) {
               slot = 0;
@@ -300,6 +333,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_in_tile = q * 32 + lane;
     const bool leader = (warp == 2 && lane == 0);
+    // the MMA CTA's accumulator-empty barrier (a remote arrive for the peer)
+    const uint32_t acc_empty0 = C::CG == 2 ? mapa_shared(smem_u32(acc_empty), 0) : 0u;
     float sab = 1.0f, sab2 = 1.0f;
     if constexpr (C::kKind == kKindE4M3) {
       sab = *ep.scale_a * *ep.scale_b;
@@ -310,52 +345,62 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     uint32_t sphase = 0;
     int it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+    for (int t = unit; t < num_tiles && ok; t += n_units, ++it) {
       const TileCoord tc = tile_coord<C::GROUP_M>(t, m_tiles, n_tiles);
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
       // one decision for all 128 threads, so no thread is left at a barrier
       if (!named_bar_and(1, C::NUM_EPI_THREADS, mbar_wait(&acc_full[buf], use, abort_flag, &g_status))) break;
       tc_fence_after_sync();
-      const int row = tc.m * C::BM + row_in_tile;
+      const int row0 = tc.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
+      const int row = row0 + row_in_tile;
+      const bool half_valid = row0 < M;  // uniform over the CTA
       float rs = 1.0f;
       if constexpr (C::kEpi != kEpiResidualPartialRms) {
         if (ep.r != nullptr) rs = row < M ? ep.r[row] : 0.0f;
       }
       const float sg = rs * sab, su = rs * sab2;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::BN);
+      auto release_acc = [&]() {
+        // last TMEM read of this tile: hand the accumulator back to the MMA warp
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (C::CG == 2) mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(buf) * 8u);
+          else mbar_arrive(&acc_empty[buf]);
+        }
+      };
+      if (!half_valid) {
+        release_acc();
+        continue;
+      }
       float ss = 0.0f;
 #pragma unroll 1
       for (int b = 0; b < C::NUM_BOXES; ++b) {
         const int col0 = tc.n * C::OUT_COLS + b * C::BOX_COLS;
-        const bool valid = col0 < N_out;  // uniform over the CTA
-        if (valid) {
-          uint32_t g[C::NC32][32];
-          uint32_t u[C::kEpi == kEpiSwiGLU ? C::NC32 : 1][32];
+        if (col0 >= N_out) break;  // uniform over the CTA
+        uint32_t g[C::NC32][32];
+        uint32_t u[C::kEpi == kEpiSwiGLU ? C::NC32 : 1][32];
 #pragma unroll
-          for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + b * C::BOX_COLS + 32 * i, g[i]);
-          if constexpr (C::kEpi == kEpiSwiGLU) {
+        for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + b * C::BOX_COLS + 32 * i, g[i]);
+        if constexpr (C::kEpi == kEpiSwiGLU) {
 #pragma unroll
-            for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + C::BN / 2 + b * C::BOX_COLS + 32 * i, u[i]);
-          }
-          tmem_wait_ld(g[0]);
+          for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + C::BN / 2 + b * C::BOX_COLS + 32 * i, u[i]);
+        }
+        tmem_wait_ld(g[0]);
 #pragma unroll
-          for (int i = 1; i < C::NC32; ++i) tmem_touch(g[i]);
-          if constexpr (C::kEpi == kEpiSwiGLU) {
+        for (int i = 1; i < C::NC32; ++i) tmem_touch(g[i]);
+        if constexpr (C::kEpi == kEpiSwiGLU) {
 #pragma unroll
-            for (int i = 0; i < C::NC32; ++i) tmem_touch(u[i]);
-          }
-          if (b == C::NUM_BOXES - 1 || tc.n * C::OUT_COLS + (b + 1) * C::BOX_COLS >= N_out) {
-            // last TMEM read of this tile: hand the accumulator back to the MMA warp
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
-          }
-          bool got = true;
-          if constexpr (C::kEpi == kEpiResidualPartialRms) got = mbar_wait(&r_full[slot], sphase, abort_flag, &g_status);
-          uint8_t* sp = slots + slot * C::SLOT_BYTES;
+          for (int i = 0; i < C::NC32; ++i) tmem_touch(u[i]);
+        }
+        if (b == C::NUM_BOXES - 1 || col0 + C::BOX_COLS >= N_out) release_acc();
+        bool got = true;
+        if constexpr (C::kEpi == kEpiResidualPartialRms) got = mbar_wait(&r_full[slot], sphase, abort_flag, &g_status);
+        uint8_t* sp = slots + slot * C::SLOT_BYTES;
+        if (got) {
 #pragma unroll
-          for (int c = 0; c < (got ? 8 : 0); ++c) {
+          for (int c = 0; c < 8; ++c) {
             float o[C::CHUNK_COLS];
 #pragma unroll
             for (int e = 0; e < C::CHUNK_COLS; ++e) {
@@ -375,7 +420,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const uint4 rv = *reinterpret_cast<const uint4*>(p);
                 const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(bf16_lo(rw[e]) + o[2 * e], bf16_hi(rw[e]) + o[2 * e + 1]);
+                for (int e = 0; e < 4; ++e)
+                  w[e] = pack_bf16x2(bf16_lo(rw[e]) + o[2 * e], bf16_hi(rw[e]) + o[2 * e + 1]);
               } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(o[2 * e], o[2 * e + 1]);
@@ -398,34 +444,34 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 v.w += rv.w;
                 ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
               }
-              if (ep.amax_out) amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+              if (ep.amax_out)
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
               *reinterpret_cast<float4*>(p) = v;
             }
           }
           if constexpr (C::kEpi == kEpiResidualPartialRms) {
             const int gcol = col0 + C::BOX_COLS;  // end column of this box
             if (gcol % kPartialCols == 0 || gcol >= N_out) {
-              const int pc = col0 / kPartialCols;
-              if (row < M) ep.P[static_cast<int64_t>(row) * ep.T + pc] = ss;
+              if (row < M) ep.P[static_cast<int64_t>(row) * ep.T + col0 / kPartialCols] = ss;
               ss = 0.0f;
             }
           }
-          // shared slot -> global
-          fence_proxy_async_smem();
-          if (!named_bar_and(1, C::NUM_EPI_THREADS, got)) {
-            ok = false;
-            break;
-          }
-          if (leader) {
-            tma_store_2d(&tmD, sp, col0, tc.m * C::BM);
-            tma_store_commit();
-            tma_store_wait_read_all();  // slot readable again before anyone rewrites it
-            if constexpr (C::kEpi == kEpiResidualPartialRms) mbar_arrive(&r_empty[slot]);
-          }
-          if (++slot == C::NSLOTS) {
-            slot = 0;
-            sphase ^= 1u;
-          }
+        }
+        // shared slot -> global
+        fence_proxy_async_smem();
+        if (!named_bar_and(1, C::NUM_EPI_THREADS, got)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          tma_store_2d(&tmD, sp, col0, row0);
+          tma_store_commit();
+          tma_store_wait_read_all();  // slot readable again before anyone rewrites it
+          if constexpr (C::kEpi == kEpiResidualPartialRms) mbar_arrive(&r_empty[slot]);
+        }
+        if (++slot == C::NSLOTS) {
+          slot = 0;
+          sphase ^= 1u;
         }
       }
     }
@@ -441,8 +487,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   // --------------------------------------------------------------- teardown ----
   tc_fence_before_sync();
   __syncthreads();
+  // a pair leaves together: no CTA frees TMEM or shared memory that the
+  // other's copies, MMAs or arrivals may still touch
+  if constexpr (C::CG == 2) cluster_sync();
   tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+  if (warp == 1) tmem_dealloc<C::CG>(tmem_base, C::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------ host ----
@@ -457,10 +506,10 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
   const uint64_t kbytes = static_cast<uint64_t>(p.K) * C::ELEM;
   const uint64_t obytes = static_cast<uint64_t>(p.N_out) * C::OUT_ELEM;
   CUresult e = encode_tmap_2d(&tmA, in_dt, p.A, p.K, p.M, kbytes, C::BK, C::BM);
-  if (e == CUDA_SUCCESS) e = encode_tmap_2d(&tmB, in_dt, p.B, p.K, p.N_out, kbytes, C::BK, C::B_ROWS_PER_LOAD);
+  if (e == CUDA_SUCCESS) e = encode_tmap_2d(&tmB, in_dt, p.B, p.K, p.N_out, kbytes, C::BK, C::B_BOX_ROWS);
   if (e == CUDA_SUCCESS)
     e = encode_tmap_2d(&tmB2, in_dt, C::kEpi == kEpiSwiGLU ? p.B2 : p.B, p.K, p.N_out, kbytes, C::BK,
-                       C::B_ROWS_PER_LOAD);
+                       C::B_BOX_ROWS);
   if (e == CUDA_SUCCESS)
     e = encode_tmap_2d(&tmR, out_dt, C::kEpi == kEpiResidualPartialRms ? p.R : p.D, p.N_out, p.M, obytes,
                        C::BOX_COLS, C::BM);
@@ -470,42 +519,86 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
     return cudaErrorInvalidValue;
   }
   auto kernel = gemm_epilogue_kernel<C>;
-  static int configured_mask = 0;  // one bit per device ordinal < 31
+  // per device: shared-memory opt-in and the number of co-resident CTA pairs
+  static int configured_mask = 0;
+  static int max_units[32] = {0};
   int dev = 0;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return ce;
-  if (dev >= 31 || !(configured_mask & (1 << dev))) {
+  if (dev >= 32 || !(configured_mask & (1 << dev))) {
     ce = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (ce != cudaSuccess) {
       *msg = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
       return ce;
     }
-    if (dev < 31) configured_mask |= 1 << dev;
+    int units = device_sm_count();
+    if (C::CG == 2) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * units);
+      cfg.blockDim = dim3(C::NUM_THREADS);
+      cfg.dynamicSmemBytes = C::SMEM_BYTES;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      ce = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(kernel), &cfg);
+      if (ce != cudaSuccess || clusters <= 0) {
+        *msg = "cudaOccupancyMaxActiveClusters failed for the CTA-pair GEMM";
+        return ce != cudaSuccess ? ce : cudaErrorInvalidConfiguration;
+      }
+      units = clusters;
+    }
+    if (dev < 32) {
+      max_units[dev] = units;
+      configured_mask |= 1 << dev;
+    }
   }
-  const int m_tiles = (p.M + C::BM - 1) / C::BM;
+  const int units = dev < 32 ? max_units[dev] : device_sm_count() / C::CG;
+  const int m_tiles = (p.M + C::TILE_M - 1) / C::TILE_M;
   const int n_tiles = (p.N_out + C::OUT_COLS - 1) / C::OUT_COLS;
   const int num_tiles = m_tiles * n_tiles;
-  const int grid = num_tiles < device_sm_count() ? num_tiles : device_sm_count();
+  const int grid = C::CG * (num_tiles < units ? num_tiles : units);
   int M = p.M, N = p.N_out, K = p.K;
   EpiParams ep = p.ep;
   void* args[] = {&tmA, &tmB, &tmB2, &tmR, &tmD, &M, &N, &K, &ep};
   ce = launch_ex(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(C::NUM_THREADS), C::SMEM_BYTES, p.stream,
-                 p.pdl, args);
+                 p.pdl, args, C::CG);
   if (ce != cudaSuccess) *msg = "GEMM kernel launch failed";
   return ce;
 }
 
-// Residual program: 3 mainloop stages + 4 R slots; the others: 4 stages + 2
-// output slots (both fit the 227 KB of shared memory per CTA).
+// CTA pairs (cta_group::2, 256-row tiles) unless the problem is too small to
+// give every pair a tile, or CODA_CTA_GROUP=1|2 forces a choice.
+inline int choose_cta_group(const GemmProblem& p) {
+  if (const char* f = getenv("CODA_CTA_GROUP")) {
+    if (f[0] == '1') return 1;
+    if (f[0] == '2') return 2;
+  }
+  const int out_cols = p.epi == kEpiSwiGLU ? 128 : 256;
+  const long tiles2 = static_cast<long>((p.M + 255) / 256) * ((p.N_out + out_cols - 1) / out_cols);
+  return tiles2 >= device_sm_count() / 2 ? 2 : 1;
+}
+
+// Shared memory per CTA (227 KB max):
+//   one CTA per MMA : 48 KB stages; residual 3 stages + 4 R slots, others 4 + 2
+//   CTA pairs       : 32 KB stages; residual 5 stages + 4 R slots, others 6 + 2
 template <int KIND>
 cudaError_t launch_gemm(const GemmProblem& p, const char** msg) {
+  const bool pair = choose_cta_group(p) == 2;
   switch (p.epi) {
     case kEpiResidualPartialRms:
-      return launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, 3, 4>>(p, msg);
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, 5, 4, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, 3, 4, 1>>(p, msg);
     case kEpiRowScale:
-      return launch_cfg<GemmCfg<KIND, kEpiRowScale, 4, 2>>(p, msg);
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiRowScale, 6, 2, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiRowScale, 4, 2, 1>>(p, msg);
     case kEpiSwiGLU:
-      return launch_cfg<GemmCfg<KIND, kEpiSwiGLU, 4, 2>>(p, msg);
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiSwiGLU, 6, 2, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiSwiGLU, 4, 2, 1>>(p, msg);
     default:
       *msg = "unknown epilogue program";
       return cudaErrorInvalidValue;
