@@ -5,7 +5,9 @@ accumulate, M = 8192 tokens (batch 4 x seq 2048):
     h = R + X Wo            X [8192, 2048], Wo [2048, 2048]   coda_gemm_residual_partial_rms
     r = rms(h)                                                 coda_rms_reduce
     act = SwiGLU(r h Wg', r h Wu')   Wg, Wu [2048, 8192]       coda_gemm_swiglu
-One step = one pass of that chain over one batch (3 kernel launches).
+One step = one pass of that chain over one batch: 2 kernel launches with the
+reduction folded into the SwiGLU GEMM's epilogue (default), 3 with
+``--reduce separate``.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl coda|reference|unfused]
 
@@ -13,7 +15,7 @@ Prints ONE JSON line (rank 0).  ``value`` is the whole-job TFLOP/s with
 inputs resident in HBM (3 rotating input sets of 136 MB each, so every step
 reads inputs that are not in the 129 MB L2); ``e2e`` is the same metric
 with the inputs copied in from pinned host memory and h and act copied back
-every step; ``roofline`` is the SwiGLU GEMM (89% of the flops) timed live
+every step (copies of one step overlapped with the compute of the next); ``roofline`` is the SwiGLU GEMM (89% of the flops) timed live
 with CUDA events around each of its launches; ``cpu_baseline`` is the fp64
 CPU oracle timed on this host on a bounded row sample.  Multi-GPU: one
 process per GPU (torchrun), each rank runs its own independent batch (weak
@@ -55,10 +57,6 @@ def peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
-
-
-def flops_swiglu_chain(M, K1, N, I):
-    return {"gemm_residual": 2.0 * M * N * K1, "swiglu": 2.0 * M * 2 * I * N}
 
 
 def algorithmic_bytes(M, K1, N, I, T):
@@ -179,27 +177,48 @@ def dist_setup(backend):
 
 # ------------------------------------------------------------- CPU oracle ----
 
+def oracle_runner(w, inp):
+    """fp64 oracle of the workload's block on a contiguous row range (rows of
+    the block are independent).  The FP8 chain's quantisation needs
+    whole-tensor scales, so on a row sample the exact chain is timed instead
+    (same GEMM shapes and work)."""
+    import oracle
+    Wt = lambda t: t.double().numpy().T.copy()  # noqa: E731
+    W = {k: Wt(inp[k]) for k in inp if k.startswith("W")}
+    G = {k: inp[k].double().numpy() for k in inp if k.startswith("gamma")}
+    X = inp["X"].double().numpy()
+    R = inp["R"].double().numpy()
+
+    def run(o, n):
+        x, r = X[o:o + n], R[o:o + n]
+        if w.chain == "swiglu":
+            oracle.block_swiglu(x, W["W1t"], r, G["gamma1"], W["Wgt"], W["Wut"], w.eps)
+        elif w.chain == "rowscale":
+            oracle.block_rowscale(x, W["W1t"], r, G["gamma1"], W["W2t"], w.eps)
+        else:
+            oracle.chain_full(x, W["W1t"], r, G["gamma1"], W["Wgt"], W["Wut"], W["Wdt"], G["gamma2"], W["Wqt"], w.eps)
+    return run
+
+
+def per_row_flops(w):
+    return sum(gemm_flops_by_kernel(w).values()) / w.M
+
+
 def oracle_sample(w, inp, budget_s, min_rows=16, max_rows=8192):
     """Time the fp64 oracle on the first rows of the workload (rows of the
     block are independent).  Returns (rows, seconds, flops, threads)."""
-    import oracle
-    Wt = lambda t: t.double().numpy().T.copy()  # noqa: E731
-    W1, Wg, Wu = Wt(inp["W1t"]), Wt(inp["Wgt"]), Wt(inp["Wut"])
-    g = inp["gamma1"].double().numpy()
-    X = inp["X"].double().numpy()
-    R = inp["R"].double().numpy()
-    per_row = 2.0 * (w.K1 * w.N + 2 * w.N * w.N2)
+    run = oracle_runner(w, inp)
 
-    def run(n):
+    def timed(n):
         t0 = time.perf_counter()
-        oracle.block_swiglu(X[:n], W1, R[:n], g, Wg, Wu, w.eps)
+        run(0, n)
         return time.perf_counter() - t0
-    run(min_rows)  # warm (thread pool, pages)
-    t = run(min_rows)
-    n = int(max(min_rows, min(max_rows, budget_s / max(t, 1e-6) * min_rows)))
-    dt = run(n)
+    timed(min_rows)  # warm (thread pool, pages)
+    t = timed(min_rows)
+    n = int(max(min_rows, min(max_rows, w.M, budget_s / max(t, 1e-6) * min_rows)))
+    dt = timed(n)
     threads = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
-    return n, dt, per_row * n, threads
+    return n, dt, per_row_flops(w) * n, threads
 
 
 # -------------------------------------------------------------- the arms ----
@@ -209,35 +228,28 @@ def run_reference(args, w):
     if rank != 0:
         return
     inp = make_inputs(w)
-    import oracle
-    Wt = lambda t: t.double().numpy().T.copy()  # noqa: E731
-    W1, Wg, Wu = Wt(inp["W1t"]), Wt(inp["Wgt"]), Wt(inp["Wut"])
-    g = inp["gamma1"].double().numpy()
-    X = inp["X"].double().numpy()
-    R = inp["R"].double().numpy()
-    per_row = 2.0 * (w.K1 * w.N + 2 * w.N * w.N2)
+    run = oracle_runner(w, inp)
     threads = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
-    # size each step's row sample so that warm-up + timed steps end in ~2 minutes
+    # size each step's row sample so that warm-up + timed steps end in about
+    # --ref-budget seconds, with at least one row per thread
     t0 = time.perf_counter()
-    oracle.block_swiglu(X[:threads], W1, R[:threads], g, Wg, Wu, w.eps)
+    run(0, threads)
     t_min = time.perf_counter() - t0
     budget = args.ref_budget / max(args.steps + args.warmup, 1)
     rows = int(max(threads, min(1024, threads * budget / max(t_min, 1e-6))))
     rows = min(rows, w.M)
     for s in range(args.warmup):
-        o = (s * rows) % (w.M - rows + 1)
-        oracle.block_swiglu(X[o:o + rows], W1, R[o:o + rows], g, Wg, Wu, w.eps)
+        run((s * rows) % (w.M - rows + 1), rows)
     t0 = time.perf_counter()
     for s in range(args.steps):
-        o = (s * rows) % (w.M - rows + 1)
-        oracle.block_swiglu(X[o:o + rows], W1, R[o:o + rows], g, Wg, Wu, w.eps)
+        run((s * rows) % (w.M - rows + 1), rows)
     dt = time.perf_counter() - t0
-    value = per_row * rows * args.steps / dt / 1e12
+    value = per_row_flops(w) * rows * args.steps / dt / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w),
+        "config": config_of(w, "separate"),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows} rows of the {w.M}-row batch per step (rows are independent), "
                                    f"fp64 unfused oracle"},
@@ -248,11 +260,160 @@ def run_reference(args, w):
 
 METRIC = "fused GEMM-epilogue chain TFLOP/s and % of GB300 dense peak; DRAM bytes vs unfused"
 
+# Per chain: the kernel the roofline reports (the one with most of the flops)
+# and the outputs an end-to-end step copies back to the host.
+DOMINANT = {"swiglu": "gemm_swiglu", "rowscale": "gemm_residual_partial_rms", "full": "gemm_swiglu"}
+E2E_OUT = {"swiglu": ("h", "act"), "rowscale": ("h", "Z"), "full": ("h2", "Z")}
 
-def config_of(w):
-    return {"workload": w.name, "chain": "gemm_residual_partial_rms -> rms_reduce -> gemm_swiglu",
-            "M": w.M, "hidden": w.N, "K1": w.K1, "intermediate": w.N2, "eps": w.eps, "seed": w.seed,
-            "l2": f"{NSETS} rotating input sets of 136 MB each (> 129 MB L2); no flush"}
+
+def chain_description(w, reduce):
+    f = reduce == "fused"
+    red = " (partials reduced to r in its epilogue)"
+    if w.chain == "swiglu":
+        return ("gemm_residual_partial_rms -> gemm_swiglu_fused_rms" + red) if f else \
+            "gemm_residual_partial_rms -> rms_reduce -> gemm_swiglu"
+    if w.chain == "rowscale":
+        return ("gemm_residual_partial_rms -> gemm_rowscale_fused_rms" + red) if f else \
+            "gemm_residual_partial_rms -> rms_reduce -> gemm_rowscale"
+    base = ("Wo: gemm_residual_partial_rms -> gate/up: gemm_swiglu -> down: gemm_residual_partial_rms (R = h1)"
+            " -> QKV: gemm_rowscale" + (", reductions fused into the consumers' epilogues" if f else
+                                        ", rms_reduce before each consumer"))
+    if w.dtype == "e4m3":
+        base = "e4m3 operands (amax + quantise of X, h1, act, h2 on the device); " + base
+    return base
+
+
+def set_bytes(w):
+    b = 1 if w.dtype == "e4m3" else 2
+    x = w.M * w.K1 * 2 + w.M * w.N * 2
+    wts = {"swiglu": w.N * w.K1 + 2 * w.N2 * w.N, "rowscale": w.N * w.K1 + w.N2 * w.N,
+           "full": w.N * w.K1 + 3 * w.inter * w.N + w.N2 * w.N}[w.chain] * b
+    return x + wts
+
+
+def config_of(w, reduce="separate"):
+    return {"workload": w.name, "chain": chain_description(w, reduce), "dtype": w.dtype,
+            "M": w.M, "hidden": w.N, "K1": w.K1, "out_or_intermediate": w.inter or w.N2, "N2": w.N2,
+            "eps": w.eps, "seed": w.seed, "heavy_rows": w.heavy_rows,
+            "l2": f"{NSETS} rotating input sets of {set_bytes(w) / 1e6:.0f} MB each (> 129 MB L2); no flush"}
+
+
+def gemm_flops_by_kernel(w):
+    M, H = w.M, w.N
+    if w.chain == "swiglu":
+        return {"gemm_residual_partial_rms": 2.0 * M * H * w.K1, "gemm_swiglu": 2.0 * M * 2 * w.N2 * H}
+    if w.chain == "rowscale":
+        return {"gemm_residual_partial_rms": 2.0 * M * H * w.K1, "gemm_rowscale": 2.0 * M * w.N2 * H}
+    return {"gemm_residual_partial_rms(Wo)": 2.0 * M * H * w.K1, "gemm_swiglu": 2.0 * M * 2 * w.inter * H,
+            "gemm_residual_partial_rms(down)": 2.0 * M * H * w.inter, "gemm_rowscale": 2.0 * M * w.N2 * H}
+
+
+def prepare_set(g, C, w, inp, dev, rank, s):
+    """Device tensors of one input set: inputs, folded (and for FP8 quantised)
+    weights, and every output buffer, so a step allocates nothing."""
+    d = {k: v.to(dev) for k, v in inp.items() if k != "heavy_idx"}
+    if s or rank:  # independent batches: same shapes and distribution, other draws
+        gen = torch.Generator(device=dev).manual_seed(1000 * rank + s + 1)
+        X = torch.randn(w.M, w.K1, generator=gen, device=dev)
+        R = torch.randn(w.M, w.N, generator=gen, device=dev)
+        if "heavy_idx" in inp:
+            idx = inp["heavy_idx"].to(dev)
+            X[idx] *= 50.0
+            R[idx] *= 50.0
+        d["X"], d["R"] = X.bfloat16(), R.bfloat16()
+    if s:  # distinct weight copies, so every step also reads its weights from HBM
+        for k in list(d):
+            if k.startswith("W"):
+                d[k] = d[k].clone()
+    gam = {k: d[k] for k in d if k.startswith("gamma")}
+    Wd = {k: d[k] for k in d if k.startswith("W")}
+    M, H = w.M, w.N
+    T = g.coda_partial_cols(H)
+    bf, f32 = torch.bfloat16, torch.float32
+    e = lambda *shape, dt=bf: torch.empty(*shape, dtype=dt, device=dev)  # noqa: E731
+    if w.chain == "swiglu":
+        f = C.fold_weights("swiglu", Wd, gam)
+        st = {"W1t": d["W1t"], "Wg": f["Wgt"], "Wu": f["Wut"], "h": e(M, H), "P": e(M, T, dt=f32), "r": e(M, dt=f32),
+              "act": e(M, w.N2)}
+    elif w.chain == "rowscale":
+        f = C.fold_weights("rowscale", Wd, gam)
+        st = {"W1t": d["W1t"], "W2": f["W2t"], "h": e(M, H), "P": e(M, T, dt=f32), "r": e(M, dt=f32), "Z": e(M, w.N2)}
+    else:
+        f = C.fold_weights("full", Wd, gam)
+        st = {"h1": e(M, H), "P1": e(M, T, dt=f32), "r1": e(M, dt=f32), "act": e(M, w.inter), "h2": e(M, H),
+              "P2": e(M, T, dt=f32), "r2": e(M, dt=f32), "Z": e(M, w.N2)}
+        if w.dtype == "e4m3":
+            st["q8"] = C.quantize_weights({"Wot": f["W1t"], "Wgt": f["Wgt"], "Wut": f["Wut"], "Wdt": f["Wdt"],
+                                           "Wqt": f["Wqt"]})
+            u8 = torch.uint8
+            st.update({"Xq": e(w.M, w.K1, dt=u8), "h1q": e(M, H, dt=u8), "actq": e(M, w.inter, dt=u8),
+                       "h2q": e(M, H, dt=u8)})
+            for k in ("ax", "a1", "a2", "a3", "sx", "s1", "s2", "s3"):
+                st[k] = e(1, dt=f32)
+        else:
+            st.update({"Wo": f["W1t"], "Wg": f["Wgt"], "Wu": f["Wut"], "Wd": f["Wdt"], "Wq": f["Wqt"]})
+    st["X"], st["R"] = d["X"], d["R"]
+    return st
+
+
+def make_step(g, C, w, fused, eps):
+    """One pass of the workload's chain over a set; ``ev`` (a pair of CUDA
+    events) brackets the dominant kernel's launch."""
+    def mark(ev, i):
+        if ev is not None:
+            ev[i].record(torch.cuda.current_stream())
+
+    def sw(h, Wg, Wu, P, r, act, ev=None, **kw):
+        mark(ev, 0)
+        if fused:
+            g.coda_gemm_swiglu_fused_rms(h, Wg, Wu, P, eps, act, r, **kw)
+        else:
+            g.coda_rms_reduce(P, h.shape[1], eps, r)
+            g.coda_gemm_swiglu(h, Wg, Wu, r, act, **kw)
+        mark(ev, 1)
+
+    def rs(h, Wq, P, r, Z, **kw):
+        if fused:
+            g.coda_gemm_rowscale_fused_rms(h, Wq, P, eps, Z, r, **kw)
+        else:
+            g.coda_rms_reduce(P, h.shape[1], eps, r)
+            g.coda_gemm_rowscale(h, Wq, r, Z, **kw)
+
+    if w.chain == "swiglu":
+        def step(st, ev=None):
+            g.coda_gemm_residual_partial_rms(st["X"], st["W1t"], st["R"], st["h"], st["P"])
+            sw(st["h"], st["Wg"], st["Wu"], st["P"], st["r"], st["act"], ev)
+        return step, (2 if fused else 3)
+    if w.chain == "rowscale":
+        def step(st, ev=None):
+            mark(ev, 0)
+            g.coda_gemm_residual_partial_rms(st["X"], st["W1t"], st["R"], st["h"], st["P"])
+            mark(ev, 1)
+            rs(st["h"], st["W2"], st["P"], st["r"], st["Z"])
+        return step, (2 if fused else 3)
+    if w.dtype != "e4m3":
+        def step(st, ev=None):
+            g.coda_gemm_residual_partial_rms(st["X"], st["Wo"], st["R"], st["h1"], st["P1"])
+            sw(st["h1"], st["Wg"], st["Wu"], st["P1"], st["r1"], st["act"], ev)
+            g.coda_gemm_residual_partial_rms(st["act"], st["Wd"], st["h1"], st["h2"], st["P2"])
+            rs(st["h2"], st["Wq"], st["P2"], st["r2"], st["Z"])
+        return step, (4 if fused else 6)
+
+    def step(st, ev=None):
+        q8 = st["q8"]
+        g.coda_amax(st["X"], st["ax"])
+        g.coda_quantize_e4m3(st["X"], st["ax"], st["Xq"], st["sx"])
+        g.coda_gemm_residual_partial_rms(st["Xq"], q8["Wot"][0], st["R"], st["h1"], st["P1"], scale_x=st["sx"],
+                                         scale_w=q8["Wot"][1], amax_h=st["a1"])
+        g.coda_quantize_e4m3(st["h1"], st["a1"], st["h1q"], st["s1"])
+        sw(st["h1q"], q8["Wgt"][0], q8["Wut"][0], st["P1"], st["r1"], st["act"], ev, scale_h=st["s1"],
+           scale_wg=q8["Wgt"][1], scale_wu=q8["Wut"][1], amax_act=st["a2"])
+        g.coda_quantize_e4m3(st["act"], st["a2"], st["actq"], st["s2"])
+        g.coda_gemm_residual_partial_rms(st["actq"], q8["Wdt"][0], st["h1"], st["h2"], st["P2"], scale_x=st["s2"],
+                                         scale_w=q8["Wdt"][1], amax_h=st["a3"])
+        g.coda_quantize_e4m3(st["h2"], st["a3"], st["h2q"], st["s3"])
+        rs(st["h2q"], q8["Wqt"][0], st["P2"], st["r2"], st["Z"], scale_h=st["s3"], scale_w=q8["Wqt"][1])
+    return step, (8 if fused else 10)
 
 
 def run_coda(args, w):
@@ -261,44 +422,19 @@ def run_coda(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import gemm_epilogue_fusion_gb300 as g
-    from gemm_epilogue_fusion_gb300 import chain
+    from gemm_epilogue_fusion_gb300 import chain as C
 
     g.load_library()
     inp = make_inputs(w)
-    M, K1, N, I = w.M, w.K1, w.N, w.N2
-    T = g.coda_partial_cols(N)
-    # independent batches per rank: same shapes, rank-specific data
-    sets = []
-    for s in range(NSETS):
-        d = {k: v.to(dev) for k, v in inp.items()}
-        if s or rank:
-            gen = torch.Generator(device=dev).manual_seed(1000 * rank + s)
-            d["X"] = torch.randn(M, K1, generator=gen, device=dev).bfloat16()
-            d["R"] = torch.randn(M, N, generator=gen, device=dev).bfloat16()
-        Wg = g.coda_fold_gamma(d["Wgt"], d["gamma1"])
-        Wu = g.coda_fold_gamma(d["Wut"], d["gamma1"])
-        if s:  # distinct weight copies so each step also reads its weights from HBM
-            d["W1t"] = d["W1t"].clone()
-        bufs = {"h": torch.empty(M, N, dtype=torch.bfloat16, device=dev),
-                "P": torch.empty(M, T, dtype=torch.float32, device=dev),
-                "r": torch.empty(M, dtype=torch.float32, device=dev),
-                "act": torch.empty(M, I, dtype=torch.bfloat16, device=dev)}
-        sets.append((d["X"], d["W1t"], d["R"], Wg, Wu, bufs))
+    sets = [prepare_set(g, C, w, inp, dev, rank, s) for s in range(NSETS)]
     torch.cuda.synchronize()
-
-    fl = flops_swiglu_chain(M, K1, N, I)
+    fused = args.reduce == "fused"
+    step, launches = make_step(g, C, w, fused, w.eps)
+    fl = gemm_flops_by_kernel(w)
     step_flops = sum(fl.values())
+    dom = DOMINANT[w.chain]
+    dom_flops = fl[dom]
     stream = torch.cuda.current_stream(dev)
-
-    def step(i, ev=None):
-        X, W1t, R, Wg, Wu, b = sets[i % NSETS]
-        h, P = g.coda_gemm_residual_partial_rms(X, W1t, R, b["h"], b["P"])
-        r = g.coda_rms_reduce(P, N, w.eps, b["r"])
-        if ev is not None:
-            ev[0].record(stream)
-        g.coda_gemm_swiglu(h, Wg, Wu, r, b["act"])
-        if ev is not None:
-            ev[1].record(stream)
 
     def barrier():
         if dist is not None:
@@ -306,9 +442,12 @@ def run_coda(args, w):
         torch.cuda.synchronize()
 
     for i in range(args.warmup):
-        step(i)
+        step(sets[i % NSETS])
     g.coda_get_device_status()
     barrier()
+    if args.profile_step:
+        profile_one_step(lambda: step(sets[args.warmup % NSETS]), rank, f"coda/{args.reduce}", launches)
+        return
 
     # ---- timed region: K steps, inputs resident in HBM
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -317,11 +456,11 @@ def run_coda(args, w):
         barrier()
         t_start.record(stream)
         for i in range(args.steps):
-            step(i, evs[i])
+            step(sets[i % NSETS], evs[i])
         t_end.record(stream)
         barrier()
     elapsed = t_start.elapsed_time(t_end) / 1e3
-    sw_ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
+    dom_ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
     g.coda_get_device_status()
     elapsed_max = elapsed
     if dist is not None:
@@ -330,30 +469,50 @@ def run_coda(args, w):
         elapsed_max = float(t.item())
     value = step_flops * args.steps * ws / elapsed_max / 1e12
 
-    # ---- end to end: pinned host inputs in, h and act out, every step
+    # ---- end to end: pinned host X, R in and the block's outputs out, every
+    # step.  Two buffer slots and three streams, so one step's copies overlap
+    # the compute of its neighbours (copy engines and SMs work concurrently).
     e2e_steps = max(10, min(200, args.steps // 10))
-    X, W1t, R, Wg, Wu, b = sets[0]
-    hX = torch.empty(X.shape, dtype=X.dtype, pin_memory=True).copy_(X.cpu())
-    hR = torch.empty(R.shape, dtype=R.dtype, pin_memory=True).copy_(R.cpu())
-    hh = torch.empty(b["h"].shape, dtype=torch.bfloat16, pin_memory=True)
-    hact = torch.empty(b["act"].shape, dtype=torch.bfloat16, pin_memory=True)
-    dX, dR = torch.empty_like(X), torch.empty_like(R)
+    outs = E2E_OUT[w.chain]
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    slots = []
+    for k in range(2):
+        st = sets[k]
+        sl = {"st": st, "in": torch.cuda.Event(), "cmp": torch.cuda.Event(), "out": torch.cuda.Event(),
+              "hX": torch.empty(st["X"].shape, dtype=st["X"].dtype, pin_memory=True).copy_(st["X"].cpu()),
+              "hR": torch.empty(st["R"].shape, dtype=st["R"].dtype, pin_memory=True).copy_(st["R"].cpu())}
+        for o in outs:
+            sl["h_" + o] = torch.empty(st[o].shape, dtype=st[o].dtype, pin_memory=True)
+        slots.append(sl)
 
-    def e2e_step():
-        dX.copy_(hX, non_blocking=True)
-        dR.copy_(hR, non_blocking=True)
-        chain.swiglu_block(dX, W1t, dR, Wg, Wu, w.eps, b)
-        hh.copy_(b["h"], non_blocking=True)
-        hact.copy_(b["act"], non_blocking=True)
+    def e2e_step(i):
+        sl = slots[i % 2]
+        st = sl["st"]
+        if i >= 2:
+            s_in.wait_event(sl["cmp"])   # step i-2 finished reading this slot's inputs
+            s_cmp.wait_event(sl["out"])  # ... and its outputs were copied out
+        with torch.cuda.stream(s_in):
+            st["X"].copy_(sl["hX"], non_blocking=True)
+            st["R"].copy_(sl["hR"], non_blocking=True)
+            sl["in"].record(s_in)
+        s_cmp.wait_event(sl["in"])
+        with torch.cuda.stream(s_cmp):
+            step(st)
+            sl["cmp"].record(s_cmp)
+        s_out.wait_event(sl["cmp"])
+        with torch.cuda.stream(s_out):
+            for o in outs:
+                sl["h_" + o].copy_(st[o], non_blocking=True)
+            sl["out"].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(4):
+        e2e_step(i)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(s_out)  # after every step's last copy (s_out runs the steps' copies in order)
     barrier()
     e2e_s = e0.elapsed_time(e1) / 1e3
     if dist is not None:
@@ -361,43 +520,61 @@ def run_coda(args, w):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
     e2e_val = step_flops * e2e_steps * ws / e2e_s / 1e12
-    h2d = hX.numel() * hX.element_size() + hR.numel() * hR.element_size()
-    d2h = hh.numel() * 2 + hact.numel() * 2
+    sl = slots[0]
+    h2d = sum(sl[k].numel() * sl[k].element_size() for k in ("hX", "hR"))
+    d2h = sum(sl["h_" + o].numel() * sl["h_" + o].element_size() for o in outs)
 
     if rank != 0:
         return
     pk, pk_kind = peaks()
-    achieved = fl["swiglu"] / (sw_ms / 1e3) / 1e12
-    fused_b, unfused_b = algorithmic_bytes(M, K1, N, I, T)
-    roof = {"kernel": "gemm_swiglu (tcgen05, bf16)", "bound": "tensor", "achieved": achieved,
-            "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-            "peak_kind": f"bf16 burst, {pk_kind}",
-            "frac_of_sustained": achieved / pk["bf16_tflops_sustained"],
-            "traffic": recorded_traffic("gemm_swiglu_llama1b"),
-            "algorithmic_bytes": fused_b["swiglu"], "avg_launch_ms": sw_ms}
+    ratio, dtname = (2.0, "e4m3 (2 x measured bf16 burst, the nominal fp8/bf16 ratio)") if w.dtype == "e4m3" else \
+        (1.0, "bf16 burst")
+    peak = pk["bf16_tflops"] * ratio
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    roof = {"kernel": f"{dom} (tcgen05, {w.dtype})", "bound": "tensor", "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": f"{dtname}, {pk_kind}",
+            "frac_of_sustained": achieved / (pk["bf16_tflops_sustained"] * ratio),
+            "traffic": recorded_traffic(f"{dom}_{w.name}"), "avg_launch_ms": dom_ms}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w),
-        "frac_of_peak": value / ws / pk["bf16_tflops"],
-        "dram_bytes_algorithmic": {"fused": sum(fused_b.values()), "unfused": unfused_b},
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if w.dtype == "e4m3" else "bf16",
+        "data": "synthetic", "config": config_of(w, args.reduce),
+        "frac_of_peak": value / ws / peak,
         "roofline": roof,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
-        "gpu_launches": 3 * args.steps,
+                "steps": e2e_steps, "how": "pinned host X, R in and " + ", ".join(outs) + " out every step; "
+                                           "2 buffer slots, copy-in / compute / copy-out streams overlapped"},
+        "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
     }
+    if w.chain == "swiglu":
+        fused_b, unfused_b = algorithmic_bytes(w.M, w.K1, w.N, w.N2, g.coda_partial_cols(w.N))
+        line["dram_bytes_algorithmic"] = {"fused": sum(fused_b.values()), "unfused": unfused_b}
+        roof["algorithmic_bytes"] = fused_b["swiglu"]
     if not args.no_cpu_baseline:
         n, dt, fl_cpu, threads = oracle_sample(w, inp, args.cpu_budget)
         line["cpu_baseline"] = {"value": fl_cpu / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                "sample": f"first {n} of {M} rows of the same batch (rows are independent), "
+                                "sample": f"first {n} of {w.M} rows of the same batch (rows are independent), "
                                           f"{dt:.1f} s of fp64 unfused oracle"}
     print(json.dumps(line), flush=True)
 
 
+def profile_one_step(step, rank, what, launches):
+    """One step between cudaProfilerStart/Stop, for `ncu --profile-from-start off`."""
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    step()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    if rank == 0:
+        print(json.dumps({"profile_step": what, "launches": launches}), flush=True)
+
+
 def run_unfused(args, w):
     """cuBLAS + PyTorch eager, unfused: XW, add, RMSNorm (fp32 math), GEMM, silu*mul."""
+    if w.chain != "swiglu":
+        raise SystemExit("--impl unfused covers the attention-out + SwiGLU block only")
     dist, rank, ws = dist_setup("nccl")
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -418,6 +595,9 @@ def run_unfused(args, w):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if args.profile_step:
+        profile_one_step(step, rank, "unfused torch eager", None)
+        return
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(args.steps):
@@ -425,11 +605,11 @@ def run_unfused(args, w):
     b.record()
     torch.cuda.synchronize()
     dt = a.elapsed_time(b) / 1e3
-    fl = sum(flops_swiglu_chain(w.M, w.K1, w.N, w.N2).values())
+    fl = sum(gemm_flops_by_kernel(w).values())
     if rank == 0:
         print(json.dumps({"impl": "unfused_torch_eager", "metric": METRIC, "value": fl * args.steps / dt / 1e12,
                           "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-                          "ms_per_step": dt / args.steps * 1e3, "dtype": "bf16", "config": config_of(w)}),
+                          "ms_per_step": dt / args.steps * 1e3, "dtype": "bf16", "config": config_of(w, "separate")}),
               flush=True)
 
 
@@ -439,8 +619,15 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["coda", "reference", "unfused"], default="coda")
-    ap.add_argument("--workload", default="llama1b_attn_out_swiglu", choices=["llama1b_attn_out_swiglu"])
+    ap.add_argument("--workload", default="llama1b_attn_out_swiglu",
+                    choices=["llama1b_attn_out_swiglu", "llama1b_mlp_down_qkv", "llama8b_chain", "llama8b_chain_fp8"],
+                    help="the default is the configuration the metric is quoted on; the others are for the "
+                         "per-configuration tables")
+    ap.add_argument("--reduce", choices=["fused", "separate"], default="fused",
+                    help="r reduced inside the SwiGLU GEMM's epilogue (2 launches per step) or by coda_rms_reduce")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="after warm-up run exactly one step inside cudaProfilerStart/Stop and exit (for ncu)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for warm-up + timed steps together")

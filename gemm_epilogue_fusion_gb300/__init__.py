@@ -48,6 +48,9 @@ SIGNATURES = {
     "coda_rms_reduce": (_i32, [_fp, _i64, _i64, _f32, _fp, _vp]),
     "coda_gemm_rowscale": (_i32, [_vp, _vp, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _vp]),
     "coda_gemm_swiglu": (_i32, [_vp, _vp, _vp, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _fp, _fp, _vp]),
+    "coda_gemm_rowscale_fused_rms": (_i32, [_vp, _vp, _fp, _f32, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _vp]),
+    "coda_gemm_swiglu_fused_rms": (_i32, [_vp, _vp, _vp, _fp, _f32, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _fp,
+                                          _fp, _vp]),
     "coda_amax": (_i32, [_vp, _i64, _i32, _fp, _vp]),
     "coda_quantize_e4m3": (_i32, [_vp, _i64, _i32, _fp, _vp, _fp, _vp]),
     "coda_get_device_status": (_i32, []),
@@ -187,6 +190,38 @@ def coda_gemm_swiglu(H, Wgt, Wut, r=None, Act=None, *, scale_h=None, scale_wg=No
     _check(lib.coda_gemm_swiglu(_dev(H, "H"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"), _dev(r, "r"), _dev(Act, "Act"),
                                 M, I, K, code, _dev(scale_h, "scale_h"), _dev(scale_wg, "scale_wg"),
                                 _dev(scale_wu, "scale_wu"), _dev(amax_act, "amax_act"), _stream(H, stream)))
+    return Act
+
+
+def coda_gemm_rowscale_fused_rms(H, W2t, P, eps: float, Z=None, r_out=None, *, scale_h=None, scale_w=None,
+                                 stream=None):
+    """Z = diag(r) H W2 with r reduced from the partials P inside the epilogue."""
+    lib = load_library()
+    M, K = H.shape
+    N2 = W2t.shape[0]
+    code = _dtype_code(H)
+    if Z is None:
+        Z = torch.empty(M, N2, dtype=_out_dtype(code), device=H.device)
+    _check(lib.coda_gemm_rowscale_fused_rms(_dev(H, "H"), _dev(W2t, "W2t"), _dev(P, "P"), float(eps),
+                                            _dev(r_out, "r_out"), _dev(Z, "Z"), M, N2, K, code,
+                                            _dev(scale_h, "scale_h"), _dev(scale_w, "scale_w"), _stream(H, stream)))
+    return Z
+
+
+def coda_gemm_swiglu_fused_rms(H, Wgt, Wut, P, eps: float, Act=None, r_out=None, *, scale_h=None, scale_wg=None,
+                               scale_wu=None, amax_act=None, stream=None):
+    """Act = silu(diag(r) H Wg) * (diag(r) H Wu) with r reduced from P inside the epilogue."""
+    lib = load_library()
+    M, K = H.shape
+    I = Wgt.shape[0]
+    code = _dtype_code(H)
+    if Act is None:
+        Act = torch.empty(M, I, dtype=_out_dtype(code), device=H.device)
+    _check(lib.coda_gemm_swiglu_fused_rms(_dev(H, "H"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"), _dev(P, "P"),
+                                          float(eps), _dev(r_out, "r_out"), _dev(Act, "Act"), M, I, K, code,
+                                          _dev(scale_h, "scale_h"), _dev(scale_wg, "scale_wg"),
+                                          _dev(scale_wu, "scale_wu"), _dev(amax_act, "amax_act"),
+                                          _stream(H, stream)))
     return Act
 
 

@@ -13,6 +13,9 @@ epilogue"; SwiGLU gate/up from the same section and "five blocks"):
                   h2 = h1 + act Wd ; r2 ; Z = diag(r2) h2 Wq'          (6 launches)
   full_chain_fp8  the same with every GEMM operand in per-tensor-scaled e4m3
 W' = diag(gamma) W is prepared once by ``fold_weights`` (coda_fold_gamma).
+With ``fused_reduce=True`` the reduction of the partials to r runs inside the
+consuming GEMM's epilogue (coda_gemm_*_fused_rms) instead of its own launch;
+r is still written out.
 Weights are W^T [N_out, K] row-major throughout.
 """
 from __future__ import annotations
@@ -21,8 +24,9 @@ from typing import Dict, Optional
 
 import torch
 
-from . import (coda_amax, coda_fold_gamma, coda_gemm_residual_partial_rms, coda_gemm_rowscale, coda_gemm_swiglu,
-               coda_quantize_e4m3, coda_rms_reduce)
+from . import (coda_amax, coda_fold_gamma, coda_gemm_residual_partial_rms, coda_gemm_rowscale,
+               coda_gemm_rowscale_fused_rms, coda_gemm_swiglu, coda_gemm_swiglu_fused_rms, coda_quantize_e4m3,
+               coda_rms_reduce)
 
 
 def _b(bufs, key):
@@ -46,28 +50,46 @@ def fold_weights(chain: str, W: Dict[str, torch.Tensor], gammas: Dict[str, torch
     return out
 
 
-def rowscale_block(X, W1t, R, W2t_folded, eps: float, bufs: Optional[dict] = None) -> dict:
+def _r_buf(bufs, key, P):
+    r = _b(bufs, key)
+    return torch.empty(P.shape[0], dtype=torch.float32, device=P.device) if r is None else r
+
+
+def _rowscale(h, Wt, P, eps, bufs, rkey, zkey, fused, **scales):
+    if fused:
+        r = _r_buf(bufs, rkey, P)
+        return coda_gemm_rowscale_fused_rms(h, Wt, P, eps, _b(bufs, zkey), r, **scales), r
+    r = coda_rms_reduce(P, h.shape[1], eps, _b(bufs, rkey))
+    return coda_gemm_rowscale(h, Wt, r, _b(bufs, zkey), **scales), r
+
+
+def _swiglu(h, Wg, Wu, P, eps, bufs, rkey, akey, fused, **kw):
+    if fused:
+        r = _r_buf(bufs, rkey, P)
+        return coda_gemm_swiglu_fused_rms(h, Wg, Wu, P, eps, _b(bufs, akey), r, **kw), r
+    r = coda_rms_reduce(P, h.shape[1], eps, _b(bufs, rkey))
+    return coda_gemm_swiglu(h, Wg, Wu, r, _b(bufs, akey), **kw), r
+
+
+def rowscale_block(X, W1t, R, W2t_folded, eps: float, bufs: Optional[dict] = None, fused_reduce=False) -> dict:
     h, P = coda_gemm_residual_partial_rms(X, W1t, R, _b(bufs, "h"), _b(bufs, "P"))
-    r = coda_rms_reduce(P, W1t.shape[0], eps, _b(bufs, "r"))
-    Z = coda_gemm_rowscale(h, W2t_folded, r, _b(bufs, "Z"))
+    Z, r = _rowscale(h, W2t_folded, P, eps, bufs, "r", "Z", fused_reduce)
     return {"h": h, "P": P, "r": r, "Z": Z}
 
 
-def swiglu_block(X, W1t, R, Wgt_folded, Wut_folded, eps: float, bufs: Optional[dict] = None) -> dict:
+def swiglu_block(X, W1t, R, Wgt_folded, Wut_folded, eps: float, bufs: Optional[dict] = None,
+                 fused_reduce=False) -> dict:
     h, P = coda_gemm_residual_partial_rms(X, W1t, R, _b(bufs, "h"), _b(bufs, "P"))
-    r = coda_rms_reduce(P, W1t.shape[0], eps, _b(bufs, "r"))
-    act = coda_gemm_swiglu(h, Wgt_folded, Wut_folded, r, _b(bufs, "act"))
+    act, r = _swiglu(h, Wgt_folded, Wut_folded, P, eps, bufs, "r", "act", fused_reduce)
     return {"h": h, "P": P, "r": r, "act": act}
 
 
-def full_chain(X, Wot, R, Wgt_f, Wut_f, Wdt, Wqt_f, eps: float, bufs: Optional[dict] = None) -> dict:
-    H = Wot.shape[0]
+def full_chain(X, Wot, R, Wgt_f, Wut_f, Wdt, Wqt_f, eps: float, bufs: Optional[dict] = None,
+               fused_reduce=False) -> dict:
     h1, P1 = coda_gemm_residual_partial_rms(X, Wot, R, _b(bufs, "h1"), _b(bufs, "P1"))
-    r1 = coda_rms_reduce(P1, H, eps, _b(bufs, "r1"))
-    act = coda_gemm_swiglu(h1, Wgt_f, Wut_f, r1, _b(bufs, "act"))
+    act, r1 = _swiglu(h1, Wgt_f, Wut_f, P1, eps, bufs, "r1", "act", fused_reduce)
     h2, P2 = coda_gemm_residual_partial_rms(act, Wdt, h1, _b(bufs, "h2"), _b(bufs, "P2"))
-    r2 = coda_rms_reduce(P2, H, eps, _b(bufs, "r2"))
-    Z = coda_gemm_rowscale(h2, Wqt_f, r2, _b(bufs, "Z"))
+    Z, r2 = _rowscale(h2, Wqt_f, P2, eps, bufs, "r2", "Z", fused_reduce)
     return {"h1": h1, "P1": P1, "r1": r1, "act": act, "h2": h2, "P2": P2, "r2": r2, "Z": Z}
 
 
@@ -79,7 +101,8 @@ def quantize_weights(W: Dict[str, torch.Tensor]) -> Dict[str, tuple]:
     return out
 
 
-def full_chain_fp8(X, R, Wq8: Dict[str, tuple], eps: float, bufs: Optional[dict] = None) -> dict:
+def full_chain_fp8(X, R, Wq8: Dict[str, tuple], eps: float, bufs: Optional[dict] = None,
+                   fused_reduce=False) -> dict:
     """FP8 chain: X, h1, act, h2 quantised per tensor on the device (amax of
     h1, act and h2 comes out of the producing GEMM's epilogue); weights from
     ``quantize_weights`` (keys Wot, Wgt, Wut, Wdt, Wqt, gamma folded)."""
@@ -93,20 +116,18 @@ def full_chain_fp8(X, R, Wq8: Dict[str, tuple], eps: float, bufs: Optional[dict]
     Wu, su = Wq8["Wut"]
     Wd, sd = Wq8["Wdt"]
     Wq, sq = Wq8["Wqt"]
-    H = Wo.shape[0]
     coda_amax(X, b["ax"])
     Xq, sx = coda_quantize_e4m3(X, b["ax"], b.get("Xq"), b.get("sx"))
     h1, P1 = coda_gemm_residual_partial_rms(Xq, Wo, R, b.get("h1"), b.get("P1"), scale_x=sx, scale_w=so,
                                             amax_h=b["a1"])
-    r1 = coda_rms_reduce(P1, H, eps, b.get("r1"))
     h1q, s1 = coda_quantize_e4m3(h1, b["a1"], b.get("h1q"), b.get("s1"))
-    act = coda_gemm_swiglu(h1q, Wg, Wu, r1, b.get("act"), scale_h=s1, scale_wg=sg, scale_wu=su, amax_act=b["a2"])
+    act, r1 = _swiglu(h1q, Wg, Wu, P1, eps, b, "r1", "act", fused_reduce, scale_h=s1, scale_wg=sg, scale_wu=su,
+                      amax_act=b["a2"])
     actq, s2 = coda_quantize_e4m3(act, b["a2"], b.get("actq"), b.get("s2"))
     h2, P2 = coda_gemm_residual_partial_rms(actq, Wd, h1, b.get("h2"), b.get("P2"), scale_x=s2, scale_w=sd,
                                             amax_h=b["a3"])
-    r2 = coda_rms_reduce(P2, H, eps, b.get("r2"))
     h2q, s3 = coda_quantize_e4m3(h2, b["a3"], b.get("h2q"), b.get("s3"))
-    Z = coda_gemm_rowscale(h2q, Wq, r2, b.get("Z"), scale_h=s3, scale_w=sq)
+    Z, r2 = _rowscale(h2q, Wq, P2, eps, b, "r2", "Z", fused_reduce, scale_h=s3, scale_w=sq)
     b.update({"Xq": Xq, "sx": sx, "h1": h1, "P1": P1, "r1": r1, "h1q": h1q, "s1": s1, "act": act, "actq": actq,
               "s2": s2, "h2": h2, "P2": P2, "r2": r2, "h2q": h2q, "s3": s3, "Z": Z})
     return b

@@ -306,22 +306,35 @@ coda_status coda_rms_reduce(const float* P, int64_t M, int64_t N, float eps, flo
   return e == cudaSuccess ? CODA_OK : cuda_fail(e, "coda_rms_reduce launch");
 }
 
-coda_status coda_gemm_rowscale(const void* H, const void* W2t, const float* r, void* Z, int64_t M, int64_t N2,
-                               int64_t K, coda_dtype dtype, const float* scale_h, const float* scale_w,
-                               cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the row-scale calls: r given, or reduced in the epilogue from P.
+coda_status gemm_rowscale_impl(const void* H, const void* W2t, const float* r, const float* P, float eps,
+                               float* r_out, void* Z, int64_t M, int64_t N2, int64_t K, coda_dtype dtype,
+                               const float* scale_h, const float* scale_w, cudaStream_t stream) {
   g_msg[0] = 0;
   TRY(check_gemm_dims(M, N2, K, dtype, "N2"));
   TRY(check_scales(dtype, scale_h, "scale_h", scale_w, "scale_w"));
+  if (P) REQUIRE(std::isfinite(eps) && eps >= 0.0f, "eps must be finite and >= 0");
   if (M == 0) return CODA_OK;
   TRY(check_ptr(H, "H"));
   TRY(check_ptr(W2t, "W2t"));
-  TRY(check_ptr(r, "r"));
   TRY(check_ptr(Z, "Z"));
+  if (P) {
+    TRY(check_ptr(P, "P"));
+    if (r_out) TRY(check_scalar_ptr(r_out, "r_out"));
+  } else {
+    TRY(check_ptr(r, "r"));
+  }
   const int ob = out_bytes(dtype), ib = elem_bytes(dtype);
-  const Range outs[] = {rng("Z", Z, M * N2 * ob)};
-  const Range ins[] = {rng("H", H, M * K * ib), rng("W2t", W2t, N2 * K * ib), rng("r", r, M * 4),
-                       rng("scale_h", scale_h, scale_h ? 4 : 0), rng("scale_w", scale_w, scale_w ? 4 : 0)};
-  TRY(check_overlaps(outs, 1, ins, 5));
+  const int64_t T = coda_partial_cols(K);
+  const Range outs[] = {rng("Z", Z, M * N2 * ob), rng("r_out", r_out, r_out ? M * 4 : 0)};
+  const Range ins[] = {rng("H", H, M * K * ib), rng("W2t", W2t, N2 * K * ib), rng("r", r, r ? M * 4 : 0),
+                       rng("P", P, P ? M * T * 4 : 0), rng("scale_h", scale_h, scale_h ? 4 : 0),
+                       rng("scale_w", scale_w, scale_w ? 4 : 0)};
+  TRY(check_overlaps(outs, 2, ins, 6));
   coda::GemmProblem p = {};
   p.epi = coda::kEpiRowScale;
   p.A = H;
@@ -330,7 +343,12 @@ coda_status coda_gemm_rowscale(const void* H, const void* W2t, const float* r, v
   p.M = static_cast<int>(M);
   p.N_out = static_cast<int>(N2);
   p.K = static_cast<int>(K);
-  p.ep.r = r;
+  p.ep.r = P ? nullptr : r;
+  p.ep.P_in = P;
+  p.ep.T_in = static_cast<int>(T);
+  p.ep.n_norm = static_cast<float>(K);
+  p.ep.eps = eps;
+  p.ep.r_out = P ? r_out : nullptr;
   p.ep.scale_a = scale_h;
   p.ep.scale_b = scale_w;
   p.stream = stream;
@@ -338,29 +356,40 @@ coda_status coda_gemm_rowscale(const void* H, const void* W2t, const float* r, v
   return run_gemm(dtype, p);
 }
 
-coda_status coda_gemm_swiglu(const void* H, const void* Wgt, const void* Wut, const float* r, void* Act, int64_t M,
-                             int64_t I, int64_t K, coda_dtype dtype, const float* scale_h, const float* scale_wg,
-                             const float* scale_wu, float* amax_act, cudaStream_t stream) {
+// Shared by the SwiGLU calls.
+coda_status gemm_swiglu_impl(const void* H, const void* Wgt, const void* Wut, const float* r, const float* P,
+                             float eps, float* r_out, void* Act, int64_t M, int64_t I, int64_t K, coda_dtype dtype,
+                             const float* scale_h, const float* scale_wg, const float* scale_wu, float* amax_act,
+                             cudaStream_t stream) {
   g_msg[0] = 0;
   TRY(check_gemm_dims(M, I, K, dtype, "I"));
   TRY(check_scales(dtype, scale_h, "scale_h", scale_wg, "scale_wg", scale_wu, "scale_wu"));
+  if (P) REQUIRE(std::isfinite(eps) && eps >= 0.0f, "eps must be finite and >= 0");
   if (amax_act) TRY(check_scalar_ptr(amax_act, "amax_act"));
   if (M == 0) return zero_scalar(amax_act, stream);
   TRY(check_ptr(H, "H"));
   TRY(check_ptr(Wgt, "Wgt"));
   TRY(check_ptr(Wut, "Wut"));
-  if (r) TRY(check_scalar_ptr(r, "r"));
+  if (P) {
+    TRY(check_ptr(P, "P"));
+    if (r_out) TRY(check_scalar_ptr(r_out, "r_out"));
+  } else if (r) {
+    TRY(check_scalar_ptr(r, "r"));
+  }
   TRY(check_ptr(Act, "Act"));
   const int ob = out_bytes(dtype), ib = elem_bytes(dtype);
-  const Range outs[] = {rng("Act", Act, M * I * ob), rng("amax_act", amax_act, amax_act ? 4 : 0)};
+  const int64_t T = coda_partial_cols(K);
+  const Range outs[] = {rng("Act", Act, M * I * ob), rng("amax_act", amax_act, amax_act ? 4 : 0),
+                        rng("r_out", r_out, r_out ? M * 4 : 0)};
   const Range ins[] = {rng("H", H, M * K * ib),
                        rng("Wgt", Wgt, I * K * ib),
                        rng("Wut", Wut, I * K * ib),
                        rng("r", r, r ? M * 4 : 0),
+                       rng("P", P, P ? M * T * 4 : 0),
                        rng("scale_h", scale_h, scale_h ? 4 : 0),
                        rng("scale_wg", scale_wg, scale_wg ? 4 : 0),
                        rng("scale_wu", scale_wu, scale_wu ? 4 : 0)};
-  TRY(check_overlaps(outs, 2, ins, 7));
+  TRY(check_overlaps(outs, 3, ins, 8));
   TRY(zero_scalar(amax_act, stream));
   coda::GemmProblem p = {};
   p.epi = coda::kEpiSwiGLU;
@@ -371,7 +400,12 @@ coda_status coda_gemm_swiglu(const void* H, const void* Wgt, const void* Wut, co
   p.M = static_cast<int>(M);
   p.N_out = static_cast<int>(I);
   p.K = static_cast<int>(K);
-  p.ep.r = r;
+  p.ep.r = P ? nullptr : r;
+  p.ep.P_in = P;
+  p.ep.T_in = static_cast<int>(T);
+  p.ep.n_norm = static_cast<float>(K);
+  p.ep.eps = eps;
+  p.ep.r_out = P ? r_out : nullptr;
   p.ep.scale_a = scale_h;
   p.ep.scale_b = scale_wg;
   p.ep.scale_b2 = scale_wu;
@@ -379,6 +413,49 @@ coda_status coda_gemm_swiglu(const void* H, const void* Wgt, const void* Wut, co
   p.stream = stream;
   p.pdl = use_pdl();
   return run_gemm(dtype, p);
+}
+
+}  // namespace
+
+extern "C" {
+
+coda_status coda_gemm_rowscale(const void* H, const void* W2t, const float* r, void* Z, int64_t M, int64_t N2,
+                               int64_t K, coda_dtype dtype, const float* scale_h, const float* scale_w,
+                               cudaStream_t stream) {
+  if (r == nullptr && M > 0) {
+    g_msg[0] = 0;
+    return fail(CODA_ERR_INVALID_ARG, "r is NULL");
+  }
+  return gemm_rowscale_impl(H, W2t, r, nullptr, 0.0f, nullptr, Z, M, N2, K, dtype, scale_h, scale_w, stream);
+}
+
+coda_status coda_gemm_rowscale_fused_rms(const void* H, const void* W2t, const float* P, float eps, float* r_out,
+                                         void* Z, int64_t M, int64_t N2, int64_t K, coda_dtype dtype,
+                                         const float* scale_h, const float* scale_w, cudaStream_t stream) {
+  if (P == nullptr && M > 0) {
+    g_msg[0] = 0;
+    return fail(CODA_ERR_INVALID_ARG, "P is NULL");
+  }
+  return gemm_rowscale_impl(H, W2t, nullptr, P, eps, r_out, Z, M, N2, K, dtype, scale_h, scale_w, stream);
+}
+
+coda_status coda_gemm_swiglu(const void* H, const void* Wgt, const void* Wut, const float* r, void* Act, int64_t M,
+                             int64_t I, int64_t K, coda_dtype dtype, const float* scale_h, const float* scale_wg,
+                             const float* scale_wu, float* amax_act, cudaStream_t stream) {
+  return gemm_swiglu_impl(H, Wgt, Wut, r, nullptr, 0.0f, nullptr, Act, M, I, K, dtype, scale_h, scale_wg, scale_wu,
+                          amax_act, stream);
+}
+
+coda_status coda_gemm_swiglu_fused_rms(const void* H, const void* Wgt, const void* Wut, const float* P, float eps,
+                                       float* r_out, void* Act, int64_t M, int64_t I, int64_t K, coda_dtype dtype,
+                                       const float* scale_h, const float* scale_wg, const float* scale_wu,
+                                       float* amax_act, cudaStream_t stream) {
+  if (P == nullptr && M > 0) {
+    g_msg[0] = 0;
+    return fail(CODA_ERR_INVALID_ARG, "P is NULL");
+  }
+  return gemm_swiglu_impl(H, Wgt, Wut, nullptr, P, eps, r_out, Act, M, I, K, dtype, scale_h, scale_wg, scale_wu,
+                          amax_act, stream);
 }
 
 coda_status coda_amax(const void* x, int64_t n, coda_dtype dtype, float* amax, cudaStream_t stream) {

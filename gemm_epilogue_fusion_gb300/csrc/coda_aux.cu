@@ -19,25 +19,16 @@ namespace coda {
 namespace {
 
 // One thread per row; a row's T partials are contiguous (16-byte loads when
-// T is a multiple of 4, which keeps every row 16-byte aligned).
+// T is a multiple of 4, which keeps every row 16-byte aligned).  The same
+// row_rstd() runs inside the row-scale and SwiGLU epilogues when they are
+// given the partials instead of r.
 __global__ void __launch_bounds__(256) rms_reduce_kernel(const float* __restrict__ P, int M, int T, float n,
                                                          float eps, float* __restrict__ r) {
   pdl_wait();
   pdl_launch_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M) return;
-  const float* p = P + static_cast<int64_t>(i) * T;
-  float s = 0.0f;
-  if ((T & 3) == 0) {
-    const float4* p4 = reinterpret_cast<const float4*>(p);
-    for (int t = 0; t < T / 4; ++t) {
-      const float4 v = __ldg(p4 + t);
-      s += (v.x + v.y) + (v.z + v.w);
-    }
-  } else {
-    for (int t = 0; t < T; ++t) s += __ldg(p + t);
-  }
-  r[i] = 1.0f / sqrtf(s / n + eps);
+  r[i] = row_rstd(P + static_cast<int64_t>(i) * T, T, n, eps);
 }
 
 // 16 bytes of W^T per thread: 8 bf16 or 4 fp32 elements of one row (K gives

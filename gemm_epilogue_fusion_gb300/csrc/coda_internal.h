@@ -7,6 +7,23 @@
 
 namespace coda {
 
+// r = 1 / sqrt(sum_t p[t] / n + eps) for one row's T partial sums of squares,
+// summed in one fixed order (16-byte groups when T % 4 == 0) so that the
+// reduction kernel and the fused epilogue give identical bits.
+__device__ __forceinline__ float row_rstd(const float* __restrict__ p, int T, float n, float eps) {
+  float s = 0.0f;
+  if ((T & 3) == 0) {
+    const float4* p4 = reinterpret_cast<const float4*>(p);
+    for (int t = 0; t < T / 4; ++t) {
+      const float4 v = __ldg(p4 + t);
+      s += (v.x + v.y) + (v.z + v.w);
+    }
+  } else {
+    for (int t = 0; t < T; ++t) s += __ldg(p + t);
+  }
+  return 1.0f / sqrtf(s / n + eps);
+}
+
 // Epilogue programs of the persistent GEMM (see gemm_epilogue.cuh).
 enum Epilogue { kEpiResidualPartialRms = 0, kEpiRowScale = 1, kEpiSwiGLU = 2 };
 
@@ -16,7 +33,14 @@ constexpr int kPartialCols = 128;
 
 // Arguments of the fused epilogue programs (all device pointers).
 struct EpiParams {
-  const float* r;         // row scale [M]: required by the row-scale program, nullable (= 1) for SwiGLU
+  const float* r;         // row scale [M]: used by the row-scale and SwiGLU programs when P_in is null
+                          // (nullable for SwiGLU: 1)
+  const float* P_in;      // row-scale / SwiGLU: partial sums of squares [M, T_in] of the previous
+                          // residual GEMM; when set, the epilogue reduces them to r itself
+  int T_in;               // columns of P_in
+  float n_norm;           // RMSNorm width N the partials cover (the GEMM's K)
+  float eps;
+  float* r_out;           // nullable: with P_in, the tiles of the first column band store r [M]
   float* P;               // residual program: partial sums of squares [M, T]
   int T;                  // columns of P
   const float* scale_a;   // E4M3 operands: dequantisation scale of A, else null

@@ -357,7 +357,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       const bool half_valid = row0 < M;  // uniform over the CTA
       float rs = 1.0f;
       if constexpr (C::kEpi != kEpiResidualPartialRms) {
-        if (ep.r != nullptr) rs = row < M ? ep.r[row] : 0.0f;
+        if (ep.P_in != nullptr) {
+          // the auxiliary reduction, folded in: this row's partials -> r
+          rs = row < M ? row_rstd(ep.P_in + static_cast<int64_t>(row) * ep.T_in, ep.T_in, ep.n_norm, ep.eps) : 0.0f;
+          if (ep.r_out != nullptr && tc.n == 0 && row < M) ep.r_out[row] = rs;
+        } else if (ep.r != nullptr) {
+          rs = row < M ? ep.r[row] : 0.0f;
+        }
       }
       const float sg = rs * sab, su = rs * sab2;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::BN);

@@ -151,6 +151,31 @@ CODA_API coda_status coda_gemm_swiglu(const void* H, const void* Wgt, const void
                              int64_t I, int64_t K, coda_dtype dtype, const float* scale_h, const float* scale_wg,
                              const float* scale_wu, float* amax_act, cudaStream_t stream);
 
+/* The auxiliary reduction folded into the second GEMM (the natural next step
+ * after section "CODA: the treasure hidden in the epilogue" calls the
+ * reduction "very light"): as coda_gemm_rowscale, except that each epilogue
+ * thread reduces its own row's partial sums of squares to r exactly as
+ * coda_rms_reduce does (same summation order, so the same bits), saving one
+ * launch and the round trip of r.
+ *   P [M, coda_partial_cols(K)] fp32: the partials written by the
+ *     coda_gemm_residual_partial_rms that produced h (RMSNorm width = K here);
+ *     for CODA_E4M3, H is the quantised h and P still comes from the bf16 h.
+ *   eps: finite, >= 0.
+ *   r_out: nullable; receives r [M] (written once per row).
+ * Other arguments as for coda_gemm_rowscale. */
+CODA_API coda_status coda_gemm_rowscale_fused_rms(const void* H, const void* W2t, const float* P, float eps,
+                                                  float* r_out, void* Z, int64_t M, int64_t N2, int64_t K,
+                                                  coda_dtype dtype, const float* scale_h, const float* scale_w,
+                                                  cudaStream_t stream);
+
+/* coda_gemm_swiglu with the reduction folded in, as for
+ * coda_gemm_rowscale_fused_rms: r is computed per row from P (K columns of h)
+ * and applied to gate and up before silu; r_out nullable. */
+CODA_API coda_status coda_gemm_swiglu_fused_rms(const void* H, const void* Wgt, const void* Wut, const float* P,
+                                                float eps, float* r_out, void* Act, int64_t M, int64_t I, int64_t K,
+                                                coda_dtype dtype, const float* scale_h, const float* scale_wg,
+                                                const float* scale_wu, float* amax_act, cudaStream_t stream);
+
 /* Per-tensor absolute maximum: *amax = max_i |x_i| over n elements of
  * dtype CODA_F32 or CODA_BF16 (overwritten).  n may be 0 (amax = 0).
  * The FP8 operands of the block's LLaMA-8B workload use per-tensor scales. */

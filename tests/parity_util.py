@@ -40,7 +40,7 @@ def to_device(inp: dict, dev="cuda") -> dict:
     return {k: v.to(dev) for k, v in inp.items() if k != "heavy_idx"}
 
 
-def run_gpu(w: Workload, d: dict) -> dict:
+def run_gpu(w: Workload, d: dict, fused_reduce: bool = False) -> dict:
     """Run the workload's block through the C ABI on device tensors ``d``;
     returns CPU copies of every output."""
     from gemm_epilogue_fusion_gb300 import chain as C
@@ -50,15 +50,16 @@ def run_gpu(w: Workload, d: dict) -> dict:
         f = C.fold_weights("full", Wd, g)
         q8 = C.quantize_weights({"Wot": f["W1t"], "Wgt": f["Wgt"], "Wut": f["Wut"], "Wdt": f["Wdt"],
                                  "Wqt": f["Wqt"]})
-        out = C.full_chain_fp8(d["X"], d["R"], q8, w.eps)
+        out = C.full_chain_fp8(d["X"], d["R"], q8, w.eps, fused_reduce=fused_reduce)
     else:
         f = C.fold_weights(w.chain, Wd, g)
         if w.chain == "rowscale":
-            out = C.rowscale_block(d["X"], d["W1t"], d["R"], f["W2t"], w.eps)
+            out = C.rowscale_block(d["X"], d["W1t"], d["R"], f["W2t"], w.eps, fused_reduce=fused_reduce)
         elif w.chain == "swiglu":
-            out = C.swiglu_block(d["X"], d["W1t"], d["R"], f["Wgt"], f["Wut"], w.eps)
+            out = C.swiglu_block(d["X"], d["W1t"], d["R"], f["Wgt"], f["Wut"], w.eps, fused_reduce=fused_reduce)
         else:
-            out = C.full_chain(d["X"], d["W1t"], d["R"], f["Wgt"], f["Wut"], d["Wdt"], f["Wqt"], w.eps)
+            out = C.full_chain(d["X"], d["W1t"], d["R"], f["Wgt"], f["Wut"], d["Wdt"], f["Wqt"], w.eps,
+                             fused_reduce=fused_reduce)
     torch.cuda.synchronize()
     return {k: v.cpu() for k, v in out.items() if isinstance(v, torch.Tensor)}
 

@@ -8,11 +8,17 @@ import pytest
 import bench
 
 
-def test_flops_of_llama1b_block():
-    fl = bench.flops_swiglu_chain(8192, 2048, 2048, 8192)
-    assert fl["gemm_residual"] == 2 * 8192 * 2048 * 2048
-    assert fl["swiglu"] == 2 * 8192 * 16384 * 2048
+def test_flops_of_each_workload():
+    from coda_inputs import WORKLOADS
+    fl = bench.gemm_flops_by_kernel(WORKLOADS["llama1b_attn_out_swiglu"])
+    assert fl["gemm_residual_partial_rms"] == 2 * 8192 * 2048 * 2048
+    assert fl["gemm_swiglu"] == 2 * 8192 * 16384 * 2048
     assert sum(fl.values()) / 1e9 == pytest.approx(618.5, abs=0.1)
+    # the per-kernel split agrees with the workload's own flop count
+    for name in ("llama1b_mlp_down_qkv", "llama8b_chain", "llama8b_chain_fp8"):
+        w = WORKLOADS[name]
+        assert sum(bench.gemm_flops_by_kernel(w).values()) == pytest.approx(w.gemm_flops())
+    assert sum(bench.gemm_flops_by_kernel(WORKLOADS["llama8b_chain"]).values()) / 1e9 == pytest.approx(7146.8, abs=1)
 
 
 def test_fused_moves_fewer_bytes_than_unfused():

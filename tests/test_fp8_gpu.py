@@ -3,6 +3,8 @@ oracle's e4m3 encoder (both deciding the code from the same fp32 quotient),
 and the LLaMA-8B FP8 chain (per-tensor scales, 5% of rows x50) against the
 quantisation-aware fp64 oracle (small M) and the exact fp64 chain on sampled
 rows (full M = 32768)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -73,19 +75,32 @@ def test_fp8_ragged_rows_and_heavy_tail():
     compare(w, got, oracle_ref(w, inp))
 
 
-def test_fp8_chain_full_size_sampled_rows():
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "llama8b_chain_fp8_rows.npz")
+
+
+def test_fp8_chain_full_size_vs_quantisation_aware_oracle():
     """M = 32768, the configuration's own size.  Per-tensor amax needs every
-    row, so the sampled rows are checked against the exact (unquantised) fp64
-    chain, which the FP8 chain must still meet within the FP8 tolerance;
-    heavy rows are in the sample."""
+    row, so the quantisation-aware oracle ran the whole chain once
+    (tests/golden/make_fp8_chain_golden.py) and stored a seeded sample of rows,
+    two of them heavy (x50).  The GPU chain must match those rows within the
+    FP8 tolerance.  Against the exact (unquantised) fp64 chain the same rows
+    differ by the e4m3 rounding of four chained GEMMs with heavy-tailed
+    scales; that error is reported and bounded loosely."""
+    import gemm_epilogue_fusion_gb300  # noqa: F401
+    from make_fp8_chain_golden import KEYS, input_digests
+    gold = np.load(GOLDEN)
     w = WORKLOADS["llama8b_chain_fp8"]
     inp = make_inputs(w)
-    d = to_device(inp)
-    got = run_gpu(w, d)
-    rows = torch.cat([sample_rows(w.M, 10), inp["heavy_idx"][:3].sort().values]).unique().sort().values
-    ref = oracle_ref(w, inp, rows)  # exact chain on these rows
+    dig = input_digests(inp)
+    assert [f"{k}:{dig[k]}" for k in KEYS] == list(gold["digests"]), "input generator changed: regenerate the golden"
+    got = run_gpu(w, to_device(inp))
+    rows = torch.from_numpy(gold["rows"])
+    ref = {k: gold[k] for k in ("h1", "r1", "act", "h2", "r2", "Z")}
     errs = compare(w, got, ref, rows)
-    print(errs)
+    exact = oracle_ref(w, inp, rows)  # exact chain on these rows
+    errs_exact = {k: oracle.rel_err(got[k][rows], exact[k]) for k in ("h1", "act", "h2", "Z")}
+    print("vs quantisation-aware oracle", errs, "vs exact chain", errs_exact)
+    assert max(errs_exact.values()) < 0.15, errs_exact
     # the fused amax outputs (GEMM epilogues) are the max |.| of what they stored
     for a, t in (("a1", "h1"), ("a2", "act"), ("a3", "h2")):
         assert float(got[a].item()) == float(got[t].float().abs().max()), a
