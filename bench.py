@@ -267,7 +267,12 @@ E2E_OUT = {"swiglu": ("h", "act"), "rowscale": ("h", "Z"), "full": ("h2", "Z")}
 
 
 def chain_description(w, reduce):
-    f = reduce == "fused"
+    if reduce == "block" and w.dtype != "e4m3":
+        if w.chain == "full":
+            return ("coda_block_swiglu (Wo + residual + partial RMS, then gate/up SwiGLU with the reduction in its "
+                    "epilogue, one persistent launch) -> coda_block_rowscale (down + residual h1, then QKV)")
+        return f"coda_block_{w.chain}: residual GEMM and its consumer in one persistent launch"
+    f = reduce != "separate"
     red = " (partials reduced to r in its epilogue)"
     if w.chain == "swiglu":
         return ("gemm_residual_partial_rms -> gemm_swiglu_fused_rms" + red) if f else \
@@ -356,12 +361,41 @@ def prepare_set(g, C, w, inp, dev, rank, s):
     return st
 
 
-def make_step(g, C, w, fused, eps):
+def make_step(g, C, w, mode, eps, ws=None):
     """One pass of the workload's chain over a set; ``ev`` (a pair of CUDA
-    events) brackets the dominant kernel's launch."""
+    events) brackets the dominant kernel's launch.  mode: "separate"
+    (rms_reduce launch), "fused" (reduction in the consumer's epilogue) or
+    "block" (residual GEMM and consumer in one persistent launch)."""
+    fused = mode != "separate"
+
     def mark(ev, i):
         if ev is not None:
             ev[i].record(torch.cuda.current_stream())
+
+    if mode == "block" and w.dtype != "e4m3":
+        if w.chain == "swiglu":
+            def step(st, ev=None):
+                mark(ev, 0)
+                g.coda_block_swiglu(st["X"], st["W1t"], st["R"], st["Wg"], st["Wu"], eps, ws, H=st["h"], P=st["P"],
+                                    Act=st["act"], r_out=st["r"])
+                mark(ev, 1)
+            return step, 1
+        if w.chain == "rowscale":
+            def step(st, ev=None):
+                mark(ev, 0)
+                g.coda_block_rowscale(st["X"], st["W1t"], st["R"], st["W2"], eps, ws, H=st["h"], P=st["P"],
+                                      Z=st["Z"], r_out=st["r"])
+                mark(ev, 1)
+            return step, 1
+
+        def step(st, ev=None):
+            mark(ev, 0)
+            g.coda_block_swiglu(st["X"], st["Wo"], st["R"], st["Wg"], st["Wu"], eps, ws, H=st["h1"], P=st["P1"],
+                                Act=st["act"], r_out=st["r1"])
+            mark(ev, 1)
+            g.coda_block_rowscale(st["act"], st["Wd"], st["h1"], st["Wq"], eps, ws, H=st["h2"], P=st["P2"],
+                                  Z=st["Z"], r_out=st["r2"])
+        return step, 2
 
     def sw(h, Wg, Wu, P, r, act, ev=None, **kw):
         mark(ev, 0)
@@ -428,12 +462,18 @@ def run_coda(args, w):
     inp = make_inputs(w)
     sets = [prepare_set(g, C, w, inp, dev, rank, s) for s in range(NSETS)]
     torch.cuda.synchronize()
-    fused = args.reduce == "fused"
-    step, launches = make_step(g, C, w, fused, w.eps)
+    mode = args.reduce if not (args.reduce == "block" and w.dtype == "e4m3") else "fused"
+    wksp = g.block_workspace(w.M, dev)
+    step, launches = make_step(g, C, w, mode, w.eps, wksp)
     fl = gemm_flops_by_kernel(w)
     step_flops = sum(fl.values())
     dom = DOMINANT[w.chain]
     dom_flops = fl[dom]
+    if mode == "block":  # the timed launch holds both GEMMs of the (first) block
+        if w.chain == "full":
+            dom, dom_flops = "block_swiglu (Wo + gate/up)", fl["gemm_residual_partial_rms(Wo)"] + fl["gemm_swiglu"]
+        else:
+            dom, dom_flops = f"block_{w.chain}", step_flops
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -446,7 +486,7 @@ def run_coda(args, w):
     g.coda_get_device_status()
     barrier()
     if args.profile_step:
-        profile_one_step(lambda: step(sets[args.warmup % NSETS]), rank, f"coda/{args.reduce}", launches)
+        profile_one_step(lambda: step(sets[args.warmup % NSETS]), rank, f"coda/{mode}", launches)
         return
 
     # ---- timed region: K steps, inputs resident in HBM
@@ -534,7 +574,7 @@ def run_coda(args, w):
     roof = {"kernel": f"{dom} (tcgen05, {w.dtype})", "bound": "tensor", "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": f"{dtname}, {pk_kind}",
             "frac_of_sustained": achieved / (pk["bf16_tflops_sustained"] * ratio),
-            "traffic": recorded_traffic(f"{dom}_{w.name}"), "avg_launch_ms": dom_ms}
+            "traffic": recorded_traffic(f"{dom.split(' ')[0]}_{w.name}"), "avg_launch_ms": dom_ms}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True,
@@ -623,8 +663,9 @@ def main():
                     choices=["llama1b_attn_out_swiglu", "llama1b_mlp_down_qkv", "llama8b_chain", "llama8b_chain_fp8"],
                     help="the default is the configuration the metric is quoted on; the others are for the "
                          "per-configuration tables")
-    ap.add_argument("--reduce", choices=["fused", "separate"], default="fused",
-                    help="r reduced inside the SwiGLU GEMM's epilogue (2 launches per step) or by coda_rms_reduce")
+    ap.add_argument("--reduce", choices=["block", "fused", "separate"], default="fused",
+                    help="block: residual GEMM and consumer in one persistent launch per block; fused: r reduced "
+                         "inside the consumer GEMM's epilogue; separate: coda_rms_reduce launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
                     help="after warm-up run exactly one step inside cudaProfilerStart/Stop and exit (for ncu)")

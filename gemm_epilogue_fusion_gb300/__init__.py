@@ -51,6 +51,11 @@ SIGNATURES = {
     "coda_gemm_rowscale_fused_rms": (_i32, [_vp, _vp, _fp, _f32, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _vp]),
     "coda_gemm_swiglu_fused_rms": (_i32, [_vp, _vp, _vp, _fp, _f32, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _fp,
                                           _fp, _vp]),
+    "coda_block_workspace_bytes": (_i64, [_i64]),
+    "coda_block_rowscale": (_i32, [_vp, _vp, _vp, _vp, _f32, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _i64, _i32, _vp,
+                                   _vp]),
+    "coda_block_swiglu": (_i32, [_vp, _vp, _vp, _vp, _vp, _f32, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _i64, _i32, _vp,
+                                 _vp]),
     "coda_amax": (_i32, [_vp, _i64, _i32, _fp, _vp]),
     "coda_quantize_e4m3": (_i32, [_vp, _i64, _i32, _fp, _vp, _fp, _vp]),
     "coda_get_device_status": (_i32, []),
@@ -223,6 +228,54 @@ def coda_gemm_swiglu_fused_rms(H, Wgt, Wut, P, eps: float, Act=None, r_out=None,
                                           _dev(scale_wu, "scale_wu"), _dev(amax_act, "amax_act"),
                                           _stream(H, stream)))
     return Act
+
+
+def coda_block_workspace_bytes(M: int) -> int:
+    return int(load_library().coda_block_workspace_bytes(M))
+
+
+def block_workspace(M: int, device) -> torch.Tensor:
+    """A zeroed workspace for the one-launch blocks (calls leave it zeroed)."""
+    n = coda_block_workspace_bytes(M)
+    return torch.zeros((n + 3) // 4, dtype=torch.int32, device=device)
+
+
+def _block_outputs(X, R, N, n_out, H, P, out, code):
+    M = X.shape[0]
+    if H is None:
+        H = torch.empty(M, N, dtype=_out_dtype(code), device=X.device)
+    if P is None:
+        P = torch.empty(M, max(coda_partial_cols(N), 0), dtype=torch.float32, device=X.device)
+    if out is None:
+        out = torch.empty(M, n_out, dtype=_out_dtype(code), device=X.device)
+    return H, P, out
+
+
+def coda_block_rowscale(X, W1t, R, W2t, eps: float, workspace, H=None, P=None, Z=None, r_out=None, stream=None):
+    """One launch: h = R + X W1, P, r, Z = diag(r) h W2 (W2t gamma-folded).  Returns (h, P, Z)."""
+    lib = load_library()
+    M, K = X.shape
+    N, N2 = W1t.shape[0], W2t.shape[0]
+    code = _dtype_code(X)
+    H, P, Z = _block_outputs(X, R, N, N2, H, P, Z, code)
+    _check(lib.coda_block_rowscale(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(W2t, "W2t"), float(eps),
+                                   _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"), _dev(Z, "Z"), M, N, K, N2, code,
+                                   _dev(workspace, "workspace"), _stream(X, stream)))
+    return H, P, Z
+
+
+def coda_block_swiglu(X, W1t, R, Wgt, Wut, eps: float, workspace, H=None, P=None, Act=None, r_out=None,
+                      stream=None):
+    """One launch: h = R + X W1, P, r, Act = silu(r h Wg) * (r h Wu).  Returns (h, P, Act)."""
+    lib = load_library()
+    M, K = X.shape
+    N, I = W1t.shape[0], Wgt.shape[0]
+    code = _dtype_code(X)
+    H, P, Act = _block_outputs(X, R, N, I, H, P, Act, code)
+    _check(lib.coda_block_swiglu(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"),
+                                 float(eps), _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"), _dev(Act, "Act"), M, N,
+                                 K, I, code, _dev(workspace, "workspace"), _stream(X, stream)))
+    return H, P, Act
 
 
 def coda_amax(x, amax=None, stream=None):

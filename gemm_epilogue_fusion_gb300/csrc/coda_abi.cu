@@ -458,6 +458,93 @@ coda_status coda_gemm_swiglu_fused_rms(const void* H, const void* Wgt, const voi
                           amax_act, stream);
 }
 
+int64_t coda_block_workspace_bytes(int64_t M) {
+  if (M < 0) return -1;
+  return ((M + 127) / 128 + 1) * static_cast<int64_t>(sizeof(unsigned));
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared by the one-launch blocks: residual GEMM (phase A) and its consumer
+// (phase B) with the reduction folded into the consumer's epilogue.
+coda_status block_impl(int epi_b, const void* X, const void* W1t, const void* R, const void* Wb, const void* Wb2,
+                       float eps, void* H, float* P, float* r_out, void* Out, int64_t M, int64_t N, int64_t K,
+                       int64_t N_out, coda_dtype dtype, void* workspace, cudaStream_t stream) {
+  g_msg[0] = 0;
+  if (dtype == CODA_E4M3)
+    return fail(CODA_ERR_UNSUPPORTED,
+                "one-launch blocks take CODA_F32 or CODA_BF16: FP8 needs the per-tensor amax of h before its consumer");
+  TRY(check_gemm_dims(M, N, K, dtype, "N"));
+  TRY(check_gemm_dims(M, N_out, N, dtype, epi_b == coda::kEpiSwiGLU ? "I" : "N2"));
+  REQUIRE(std::isfinite(eps) && eps >= 0.0f, "eps must be finite and >= 0");
+  if (M == 0) return CODA_OK;
+  TRY(check_ptr(X, "X"));
+  TRY(check_ptr(W1t, "W1t"));
+  TRY(check_ptr(R, "R"));
+  TRY(check_ptr(Wb, epi_b == coda::kEpiSwiGLU ? "Wgt" : "W2t"));
+  if (epi_b == coda::kEpiSwiGLU) TRY(check_ptr(Wb2, "Wut"));
+  TRY(check_ptr(H, "H"));
+  TRY(check_ptr(P, "P"));
+  if (r_out) TRY(check_scalar_ptr(r_out, "r_out"));
+  TRY(check_ptr(Out, epi_b == coda::kEpiSwiGLU ? "Act" : "Z"));
+  TRY(check_ptr(workspace, "workspace"));
+  const int ob = out_bytes(dtype), ib = elem_bytes(dtype);
+  const int64_t T = coda_partial_cols(N);
+  const Range outs[] = {rng("H", H, M * N * ob), rng("P", P, M * T * 4), rng("r_out", r_out, r_out ? M * 4 : 0),
+                        rng(epi_b == coda::kEpiSwiGLU ? "Act" : "Z", Out, M * N_out * ob),
+                        rng("workspace", workspace, coda_block_workspace_bytes(M))};
+  const Range ins[] = {rng("X", X, M * K * ib), rng("W1t", W1t, N * K * ib), rng("R", R, M * N * ob),
+                       rng("W", Wb, N_out * N * ib), rng("Wut", Wb2, Wb2 ? N_out * N * ib : 0)};
+  TRY(check_overlaps(outs, 5, ins, 5));
+  coda::GemmProblem p = {};
+  p.epi = coda::kEpiResidualPartialRms;
+  p.A = X;
+  p.B = W1t;
+  p.R = R;
+  p.D = H;
+  p.M = static_cast<int>(M);
+  p.N_out = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.ep.P = P;
+  p.ep.T = static_cast<int>(T);
+  p.b.epi = epi_b;
+  p.b.A = H;
+  p.b.B = Wb;
+  p.b.B2 = Wb2;
+  p.b.D = Out;
+  p.b.N_out = static_cast<int>(N_out);
+  p.b.K = static_cast<int>(N);
+  p.b.ep.P_in = P;
+  p.b.ep.T_in = static_cast<int>(T);
+  p.b.ep.n_norm = static_cast<float>(N);
+  p.b.ep.eps = eps;
+  p.b.ep.r_out = r_out;
+  p.band_ready = static_cast<unsigned*>(workspace);
+  p.stream = stream;
+  p.pdl = use_pdl();
+  return run_gemm(dtype, p);
+}
+
+}  // namespace
+
+extern "C" {
+
+coda_status coda_block_rowscale(const void* X, const void* W1t, const void* R, const void* W2t, float eps, void* H,
+                                float* P, float* r_out, void* Z, int64_t M, int64_t N, int64_t K, int64_t N2,
+                                coda_dtype dtype, void* workspace, cudaStream_t stream) {
+  return block_impl(coda::kEpiRowScale, X, W1t, R, W2t, nullptr, eps, H, P, r_out, Z, M, N, K, N2, dtype, workspace,
+                    stream);
+}
+
+coda_status coda_block_swiglu(const void* X, const void* W1t, const void* R, const void* Wgt, const void* Wut,
+                              float eps, void* H, float* P, float* r_out, void* Act, int64_t M, int64_t N, int64_t K,
+                              int64_t I, coda_dtype dtype, void* workspace, cudaStream_t stream) {
+  return block_impl(coda::kEpiSwiGLU, X, W1t, R, Wgt, Wut, eps, H, P, r_out, Act, M, N, K, I, dtype, workspace,
+                    stream);
+}
+
 coda_status coda_amax(const void* x, int64_t n, coda_dtype dtype, float* amax, cudaStream_t stream) {
   g_msg[0] = 0;
   REQUIRE(dtype == CODA_F32 || dtype == CODA_BF16, "coda_amax: dtype must be CODA_F32 or CODA_BF16");

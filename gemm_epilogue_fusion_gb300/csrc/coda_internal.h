@@ -49,6 +49,17 @@ struct EpiParams {
   float* amax_out;        // nullable: max |stored output|, combined with atomicMax (caller zeroes it)
 };
 
+// Second phase of a two-phase launch (the consuming GEMM of the block).
+struct PhaseB {
+  int epi = -1;            // kEpiRowScale or kEpiSwiGLU; -1 = one-phase launch
+  const void* A = nullptr;  // h [M, K] (phase A's output)
+  const void* B = nullptr;  // weight [N_out, K]; SwiGLU: gate weight
+  const void* B2 = nullptr; // SwiGLU: up weight
+  void* D = nullptr;        // output [M, N_out]
+  int N_out = 0, K = 0;
+  EpiParams ep = {};
+};
+
 struct GemmProblem {
   int epi;                 // Epilogue
   const void* A;           // [M, K] K-major activations
@@ -60,6 +71,8 @@ struct GemmProblem {
   EpiParams ep;
   cudaStream_t stream;
   bool pdl;                // launch with programmatic stream serialisation
+  PhaseB b;                // consuming GEMM of a two-phase launch
+  unsigned* band_ready;    // two-phase: [ceil(M / tile rows) + 1] zeroed counters
 };
 
 // One launcher per operand kind; each lives in its own translation unit so

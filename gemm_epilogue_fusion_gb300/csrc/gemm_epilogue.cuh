@@ -4,7 +4,8 @@
 // (activations [M, K] and weights W^T [N_out, K], row-major), TMA-loaded with
 // 128-byte swizzle so every k-block row of a tile is exactly 128 bytes.
 //
-// One CTA per SM walks 128-row output tiles.  Roles (warps):
+// One CTA (or one cluster pair of CTAs, tcgen05 cta_group::2) per SM walks
+// output tiles of 128 (256) rows.  Roles (warps):
 //   0      TMA producer: A and B k-blocks into a STAGES-deep shared ring
 //   1      TMEM owner + MMA issuer (one thread): tcgen05.mma into one of two
 //          256-column TMEM accumulators, so the epilogue of tile i overlaps
@@ -12,8 +13,10 @@
 //   2..5   epilogue: tcgen05.ld (one accumulator row per thread) -> fused
 //          program -> 128B-swizzled shared slot -> TMA store, one 128-byte
 //          wide column box at a time
-//   6      residual program only: TMA loads of R boxes into the slot ring, so
-//          the residual add reads R from shared memory and writes h in place
+//   6      residual program: TMA loads of R boxes into the slot ring, so the
+//          residual add reads R from shared memory and writes h in place; in
+//          a two-phase launch it also hands the slots of the second phase's
+//          boxes to the epilogue
 //
 // Epilogue programs.  The CODA write-ups ("CODA: the treasure hidden in the
 // epilogue") apply the memory-bound neighbours of a GEMM while its product is
@@ -27,10 +30,21 @@
 //                           accumulators of the same 128 output columns share
 //                           one N=256 MMA (B tile = 128 gate rows ++ 128 up rows).
 // E4M3 operands: acc is multiplied by the per-tensor scales of A and B first.
+//
+// Two-phase launch (the whole GEMM -> RMSNorm -> GEMM block in one persistent
+// kernel): the tile sequence is every residual-GEMM tile (phase A), then every
+// tile of the consuming row-scale or SwiGLU GEMM (phase B, its r reduced from
+// P in the epilogue).  A phase-B tile of row band m waits until every phase-A
+// tile of band m has stored its h and P (a per-band counter in global memory,
+// released after the stores complete, acquired before the TMA loads of h), so
+// the consuming GEMM fills the SMs the residual GEMM's last wave leaves idle.
+// All phase-A tiles precede all phase-B tiles in every CTA's walk and the grid
+// is co-resident, so the waits cannot form a cycle.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cstdlib>
+#include <type_traits>
 
 #include "coda_internal.h"
 #include "sm103_ptx.cuh"
@@ -43,10 +57,15 @@ namespace {
 __device__ unsigned g_status;
 }
 
-template <int KIND, int EPI, int STAGES_, int NSLOTS_, int CG_ = 1>
+constexpr int kNoPhase = -1;
+
+template <int KIND, int EPI_A, int EPI_B, int STAGES_, int NSLOTS_, int CG_ = 1>
 struct GemmCfg {
   static constexpr int kKind = KIND;
-  static constexpr int kEpi = EPI;
+  static constexpr int kEpiA = EPI_A;         // program of the (first) phase
+  static constexpr int kEpiB = EPI_B;         // program of the second phase, or kNoPhase
+  static constexpr bool TWO_PHASE = EPI_B != kNoPhase;
+  static constexpr bool HAS_LOADER = EPI_A == kEpiResidualPartialRms;  // warp 6 owns the slot ring
   static constexpr int CG = CG_;              // CTAs per MMA (cta_group::1 or ::2)
   static constexpr int BM = 128;              // accumulator rows per CTA
   static constexpr int TILE_M = BM * CG;      // output rows per tile (per CTA pair)
@@ -61,19 +80,19 @@ struct GemmCfg {
   static constexpr int B_ROWS = BN / CG;    // B rows held by this CTA
   static constexpr int B_BYTES = B_ROWS * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // this CTA's bytes per stage
+  // output columns per tile of a program
+  __host__ __device__ static constexpr int out_cols(int epi) { return epi == kEpiSwiGLU ? BN / 2 : BN; }
   // rows of one B TMA box: SwiGLU with one CTA loads gate and up halves
   // separately; with a pair, each CTA loads one of them whole
-  static constexpr int B_BOX_ROWS = (EPI == kEpiSwiGLU && CG == 1) ? BN / 2 : B_ROWS;
-  static constexpr int OUT_COLS = EPI == kEpiSwiGLU ? BN / 2 : BN;  // output columns per tile
-  static constexpr int OUT_ELEM = KIND == kKindTF32 ? 4 : 2;         // fp32 out for tf32, else bf16
-  static constexpr int BOX_COLS = 128 / OUT_ELEM;                    // output columns per 128-byte box
-  static constexpr int NUM_BOXES = OUT_COLS / BOX_COLS;
+  __host__ __device__ static constexpr int b_box_rows(int epi) { return (epi == kEpiSwiGLU && CG == 1) ? BN / 2 : B_ROWS; }
+  static constexpr int OUT_ELEM = KIND == kKindTF32 ? 4 : 2;  // fp32 out for tf32, else bf16
+  static constexpr int BOX_COLS = 128 / OUT_ELEM;             // output columns per 128-byte box
   static constexpr int NC32 = BOX_COLS / 32;  // 32-column TMEM loads per box (per operand half)
   static constexpr int CHUNK_COLS = 16 / OUT_ELEM;  // columns per 16-byte chunk of a box row
   static constexpr int SLOT_BYTES = BM * 128;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int NUM_EPI_THREADS = 128;
-  static constexpr int NUM_THREADS = EPI == kEpiResidualPartialRms ? 224 : 192;
+  static constexpr int NUM_THREADS = HAS_LOADER ? 224 : 192;
   static constexpr int GROUP_M = 16 / CG;  // tile raster: 2048-row bands share each B panel in flight
   // shared memory: [A stages][B stages][slots][barriers][tmem slot, abort flag]
   static constexpr int OFF_B = STAGES * A_BYTES;
@@ -82,9 +101,11 @@ struct GemmCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * NSLOTS + 1;
   static constexpr int SMEM_BYTES = OFF_BARS + NUM_BARS * 8 + 16 + 1024;  // + slack for 1 KB alignment
   static_assert(CG == 1 || CG == 2, "CTA group");
+  static_assert(!TWO_PHASE || (EPI_A == kEpiResidualPartialRms && (EPI_B == kEpiRowScale || EPI_B == kEpiSwiGLU)),
+                "a two-phase launch is residual GEMM -> row-scale or SwiGLU GEMM");
   static_assert(TMEM_COLS == 512, "two 256-column accumulators");
-  static_assert(OUT_COLS % BOX_COLS == 0 && BOX_COLS % 32 == 0, "box tiling");
-  static_assert(kPartialCols % BOX_COLS == 0 && OUT_COLS % kPartialCols == 0, "partial groups");
+  static_assert((BN / 2) % BOX_COLS == 0 && BOX_COLS % 32 == 0, "box tiling");
+  static_assert(kPartialCols % BOX_COLS == 0 && BN % kPartialCols == 0, "partial groups");
   static_assert(NSLOTS >= 2, "slot ring");
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory");
   static constexpr uint32_t FMT = KIND == kKindBF16 ? 1u : (KIND == kKindTF32 ? 2u : 0u);
@@ -106,6 +127,22 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int m_tiles, int n_tiles)
   const int gm = min(GROUP_M, m_tiles - first_m);
   const int local = t - g * per_group;
   return {first_m + local % gm, local / gm};
+}
+
+// Position of tile index t in the launch's walk: phase A tiles first.
+struct Tile {
+  int phase;  // 0 = A, 1 = B
+  int m, n;
+};
+template <int GROUP_M>
+__device__ __forceinline__ Tile tile_at(int t, int m_tiles, int n_tiles_a, int n_tiles_b) {
+  const int num_a = m_tiles * n_tiles_a;
+  if (t < num_a) {
+    const TileCoord c = tile_coord<GROUP_M>(t, m_tiles, n_tiles_a);
+    return {0, c.m, c.n};
+  }
+  const TileCoord c = tile_coord<GROUP_M>(t - num_a, m_tiles, n_tiles_b);
+  return {1, c.m, c.n};
 }
 
 // silu(x) = x * sigmoid(x) = x / (1 + e^-x); for x -> -inf the quotient
@@ -137,11 +174,39 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int n_stages, uint32_
   }
 }
 
+// Band dependency of a two-phase launch: spin (bounded) until the counter
+// reaches `target`, with acquire semantics at GPU scope.
+__device__ __forceinline__ bool wait_band(const unsigned* ctr, unsigned target, volatile int* abort_flag) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > CODA_WAIT_TIMEOUT_NS) {
+        *abort_flag = 1;
+        atomicOr(&g_status, kDevTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Operands of one phase.
+struct PhaseArgs {
+  int N_out, K;
+  EpiParams ep;
+};
+
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmR,
-                         const __grid_constant__ CUtensorMap tmD, int M, int N_out, int K, EpiParams ep) {
+                         const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmA_b,
+                         const __grid_constant__ CUtensorMap tmB_b, const __grid_constant__ CUtensorMap tmB2_b,
+                         const __grid_constant__ CUtensorMap tmD_b, int M, PhaseArgs pa, PhaseArgs pb,
+                         unsigned* band_ready) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -167,9 +232,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   const int unit = blockIdx.x / C::CG;     // tile-walking unit (a CTA or a CTA pair)
   const int n_units = gridDim.x / C::CG;
   const int m_tiles = (M + C::TILE_M - 1) / C::TILE_M;
-  const int n_tiles = (N_out + C::OUT_COLS - 1) / C::OUT_COLS;
-  const int num_tiles = m_tiles * n_tiles;
-  const int num_kb = (K + C::BK - 1) / C::BK;
+  const int n_tiles_a = (pa.N_out + C::out_cols(C::kEpiA) - 1) / C::out_cols(C::kEpiA);
+  const int n_tiles_b = C::TWO_PHASE ? (pb.N_out + C::out_cols(C::kEpiB) - 1) / C::out_cols(C::kEpiB) : 0;
+  const int num_tiles = m_tiles * (n_tiles_a + n_tiles_b);
+  // a band is ready for phase B when every phase-A tile of it (one increment
+  // per CTA) has stored h and P
+  const unsigned band_target = static_cast<unsigned>(n_tiles_a * C::CG);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -191,9 +259,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if constexpr (C::kEpi == kEpiSwiGLU) tma_prefetch_desc(&tmB2);
-    if constexpr (C::kEpi == kEpiResidualPartialRms) tma_prefetch_desc(&tmR);
+    if constexpr (C::kEpiA == kEpiSwiGLU) tma_prefetch_desc(&tmB2);
+    if constexpr (C::HAS_LOADER) tma_prefetch_desc(&tmR);
     tma_prefetch_desc(&tmD);
+    if constexpr (C::TWO_PHASE) {
+      tma_prefetch_desc(&tmA_b);
+      tma_prefetch_desc(&tmB_b);
+      if constexpr (C::kEpiB == kEpiSwiGLU) tma_prefetch_desc(&tmB2_b);
+      tma_prefetch_desc(&tmD_b);
+    }
   }
   if (warp == 1) {
     tmem_alloc<C::CG>(tmem_slot, C::TMEM_COLS);
@@ -220,8 +294,19 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       uint32_t phase = 0, issued = 0;
       bool ok = true;
       for (int t = unit; t < num_tiles && ok; t += n_units) {
-        const TileCoord tc = tile_coord<C::GROUP_M>(t, m_tiles, n_tiles);
-        const int a_row = tc.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
+        const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
+        const bool pB = C::TWO_PHASE && tl.phase == 1;
+        const CUtensorMap* mA = pB ? &tmA_b : &tmA;
+        const CUtensorMap* mB = pB ? &tmB_b : &tmB;
+        const CUtensorMap* mB2 = pB ? &tmB2_b : &tmB2;
+        const bool swiglu = pB ? C::kEpiB == kEpiSwiGLU : C::kEpiA == kEpiSwiGLU;
+        const int num_kb = ((pB ? pb.K : pa.K) + C::BK - 1) / C::BK;
+        const int a_row = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
+        if (pB) {
+          // h and P of this band come from other CTAs of this launch
+          if (!wait_band(&band_ready[tl.m], band_target, abort_flag)) break;
+          fence_proxy_async_global();
+        }
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_status)) {
             ok = false;
@@ -232,19 +317,22 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           uint8_t* b = sB + stage * C::B_BYTES;
           if constexpr (C::CG == 1) {
             mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-            tma_load_2d(a, &tmA, &full[stage], kx, a_row, pol);
-            tma_load_2d(b, &tmB, &full[stage], kx, tc.n * C::B_BOX_ROWS, pol);
-            if constexpr (C::kEpi == kEpiSwiGLU)
-              tma_load_2d(b + C::B_BOX_ROWS * 128, &tmB2, &full[stage], kx, tc.n * C::B_BOX_ROWS, pol);
+            tma_load_2d(a, mA, &full[stage], kx, a_row, pol);
+            if (swiglu) {
+              tma_load_2d(b, mB, &full[stage], kx, tl.n * (C::BN / 2), pol);
+              tma_load_2d(b + (C::BN / 2) * 128, mB2, &full[stage], kx, tl.n * (C::BN / 2), pol);
+            } else {
+              tma_load_2d(b, mB, &full[stage], kx, tl.n * C::BN, pol);
+            }
           } else {
             // the MMA CTA expects both CTAs' bytes; the peer only issues its copies
             if (mma_cta) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
             const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
-            tma_load_2d_pair(a, &tmA, fb, kx, a_row, pol);
-            if constexpr (C::kEpi == kEpiSwiGLU)  // rank 0: gate rows, rank 1: up rows
-              tma_load_2d_pair(b, cta_rank == 0 ? &tmB : &tmB2, fb, kx, tc.n * C::B_ROWS, pol);
+            tma_load_2d_pair(a, mA, fb, kx, a_row, pol);
+            if (swiglu)  // rank 0: gate rows, rank 1: up rows
+              tma_load_2d_pair(b, cta_rank == 0 ? mB : mB2, fb, kx, tl.n * C::B_ROWS, pol);
             else
-              tma_load_2d_pair(b, &tmB, fb, kx, tc.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS, pol);
+              tma_load_2d_pair(b, mB, fb, kx, tl.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS, pol);
           }
           ++issued;
           if (++stage == C::STAGES) {
@@ -266,6 +354,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int t = unit; t < num_tiles && ok; t += n_units, ++it) {
+        const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
+        const int num_kb = (((C::TWO_PHASE && tl.phase == 1) ? pb.K : pa.K) + C::BK - 1) / C::BK;
         const int buf = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
         if (!mbar_wait(&acc_empty[buf], use ^ 1u, abort_flag, &g_status)) break;
@@ -298,34 +388,44 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       (void)mbar_wait(mma_drain, 0, abort_flag, &g_status, false);
     }
   } else if (warp == 6) {
-    // ----------------------------------------- residual loader (R boxes) ----
-    if constexpr (C::kEpi == kEpiResidualPartialRms) {
+    // ------------------------------------------------ slot ring (R boxes) ----
+    // Residual boxes: TMA-load R into the slot.  Boxes of a second phase:
+    // hand the free slot to the epilogue as output staging.
+    if constexpr (C::HAS_LOADER) {
       if (lane == 0) {
         const uint64_t pol = l2_policy_evict_first();
         int slot = 0;
-        uint32_t phase = 0, issued = 0;
+        uint32_t phase = 0, used = 0;
         bool ok = true;
         for (int t = unit; t < num_tiles && ok; t += n_units) {
-          const TileCoord tc = tile_coord<C::GROUP_M>(t, m_tiles, n_tiles);
-          const int row0 = tc.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
+          const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
+          const bool pB = C::TWO_PHASE && tl.phase == 1;
+          const int row0 = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
           if (row0 >= M) continue;  // this CTA's half of the tile is empty
-          for (int b = 0; b < C::NUM_BOXES; ++b) {
-            const int col0 = tc.n * C::OUT_COLS + b * C::BOX_COLS;
-            if (col0 >= N_out) break;
+          const int oc = pB ? C::out_cols(C::kEpiB) : C::out_cols(C::kEpiA);
+          const int n_out = pB ? pb.N_out : pa.N_out;
+          for (int b = 0; b < oc / C::BOX_COLS; ++b) {
+            const int col0 = tl.n * oc + b * C::BOX_COLS;
+            if (col0 >= n_out) break;
             if (!mbar_wait(&r_empty[slot], phase ^ 1u, abort_flag, &g_status)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&r_full[slot], C::SLOT_BYTES);
-            tma_load_2d(slots + slot * C::SLOT_BYTES, &tmR, &r_full[slot], col0, row0, pol);
-            ++issued;
+            if (pB) {
+              mbar_arrive(&r_full[slot]);
+            } else {
+              mbar_arrive_expect_tx(&r_full[slot], C::SLOT_BYTES);
+              tma_load_2d(slots + slot * C::SLOT_BYTES, &tmR, &r_full[slot], col0, row0, pol);
+            }
+            ++used;
             if (++slot == C::NSLOTS) {
               slot = 0;
               phase ^= 1u;
             }
           }
         }
-        drain_ring(r_full, C::NSLOTS, issued, abort_flag);
+        // every R load issued must land before exit (hand-overs complete at once)
+        drain_ring(r_full, C::NSLOTS, used, abort_flag);
       }
     }
   } else {
@@ -335,32 +435,34 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const bool leader = (warp == 2 && lane == 0);
     // the MMA CTA's accumulator-empty barrier (a remote arrive for the peer)
     const uint32_t acc_empty0 = C::CG == 2 ? mapa_shared(smem_u32(acc_empty), 0) : 0u;
-    float sab = 1.0f, sab2 = 1.0f;
-    if constexpr (C::kKind == kKindE4M3) {
-      sab = *ep.scale_a * *ep.scale_b;
-      if constexpr (C::kEpi == kEpiSwiGLU) sab2 = *ep.scale_a * *ep.scale_b2;
-    }
     float amax = 0.0f;
     int slot = 0;
     uint32_t sphase = 0;
     int it = 0;
     bool ok = true;
-    for (int t = unit; t < num_tiles && ok; t += n_units, ++it) {
-      const TileCoord tc = tile_coord<C::GROUP_M>(t, m_tiles, n_tiles);
-      const int buf = it & 1;
-      const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
-      // one decision for all 128 threads, so no thread is left at a barrier
-      if (!named_bar_and(1, C::NUM_EPI_THREADS, mbar_wait(&acc_full[buf], use, abort_flag, &g_status))) break;
-      tc_fence_after_sync();
-      const int row0 = tc.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
+
+    // One tile of program EPI: TMEM -> program -> slot -> TMA store, box by box.
+    auto run_tile = [&](auto epi_tag, const Tile& tl, const PhaseArgs& ph, const CUtensorMap* mD, int buf) {
+      constexpr int EPI = decltype(epi_tag)::value;
+      constexpr int OUT_COLS = C::out_cols(EPI);
+      constexpr int NUM_BOXES = OUT_COLS / C::BOX_COLS;
+      const EpiParams& ep = ph.ep;
+      const int N_out = ph.N_out;
+      float sab = 1.0f, sab2 = 1.0f;
+      if constexpr (C::kKind == kKindE4M3) {
+        sab = *ep.scale_a * *ep.scale_b;
+        if constexpr (EPI == kEpiSwiGLU) sab2 = *ep.scale_a * *ep.scale_b2;
+      }
+      const int row0 = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
       const int row = row0 + row_in_tile;
       const bool half_valid = row0 < M;  // uniform over the CTA
       float rs = 1.0f;
-      if constexpr (C::kEpi != kEpiResidualPartialRms) {
+      if constexpr (EPI != kEpiResidualPartialRms) {
         if (ep.P_in != nullptr) {
           // the auxiliary reduction, folded in: this row's partials -> r
+          if constexpr (C::TWO_PHASE) (void)wait_band(&band_ready[tl.m], band_target, abort_flag);  // acquire P
           rs = row < M ? row_rstd(ep.P_in + static_cast<int64_t>(row) * ep.T_in, ep.T_in, ep.n_norm, ep.eps) : 0.0f;
-          if (ep.r_out != nullptr && tc.n == 0 && row < M) ep.r_out[row] = rs;
+          if (ep.r_out != nullptr && tl.n == 0 && row < M) ep.r_out[row] = rs;
         } else if (ep.r != nullptr) {
           rs = row < M ? ep.r[row] : 0.0f;
         }
@@ -378,31 +480,34 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       };
       if (!half_valid) {
         release_acc();
-        continue;
+        // nothing to store, but the band still counts this CTA's share of the tile
+        if constexpr (C::TWO_PHASE && EPI == kEpiResidualPartialRms)
+          if (leader) red_release_gpu_add(&band_ready[tl.m], 1u);
+        return;
       }
       float ss = 0.0f;
 #pragma unroll 1
-      for (int b = 0; b < C::NUM_BOXES; ++b) {
-        const int col0 = tc.n * C::OUT_COLS + b * C::BOX_COLS;
+      for (int b = 0; b < NUM_BOXES; ++b) {
+        const int col0 = tl.n * OUT_COLS + b * C::BOX_COLS;
         if (col0 >= N_out) break;  // uniform over the CTA
         uint32_t g[C::NC32][32];
-        uint32_t u[C::kEpi == kEpiSwiGLU ? C::NC32 : 1][32];
+        uint32_t u[EPI == kEpiSwiGLU ? C::NC32 : 1][32];
 #pragma unroll
         for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + b * C::BOX_COLS + 32 * i, g[i]);
-        if constexpr (C::kEpi == kEpiSwiGLU) {
+        if constexpr (EPI == kEpiSwiGLU) {
 #pragma unroll
           for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + C::BN / 2 + b * C::BOX_COLS + 32 * i, u[i]);
         }
         tmem_wait_ld(g[0]);
 #pragma unroll
         for (int i = 1; i < C::NC32; ++i) tmem_touch(g[i]);
-        if constexpr (C::kEpi == kEpiSwiGLU) {
+        if constexpr (EPI == kEpiSwiGLU) {
 #pragma unroll
           for (int i = 0; i < C::NC32; ++i) tmem_touch(u[i]);
         }
-        if (b == C::NUM_BOXES - 1 || col0 + C::BOX_COLS >= N_out) release_acc();
+        if (b == NUM_BOXES - 1 || col0 + C::BOX_COLS >= N_out) release_acc();
         bool got = true;
-        if constexpr (C::kEpi == kEpiResidualPartialRms) got = mbar_wait(&r_full[slot], sphase, abort_flag, &g_status);
+        if constexpr (C::HAS_LOADER) got = mbar_wait(&r_full[slot], sphase, abort_flag, &g_status);
         uint8_t* sp = slots + slot * C::SLOT_BYTES;
         if (got) {
 #pragma unroll
@@ -412,7 +517,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             for (int e = 0; e < C::CHUNK_COLS; ++e) {
               const int j = c * C::CHUNK_COLS + e;
               const float a = __uint_as_float(g[j >> 5][j & 31]);
-              if constexpr (C::kEpi == kEpiSwiGLU) {
+              if constexpr (EPI == kEpiSwiGLU) {
                 const float uu = __uint_as_float(u[j >> 5][j & 31]);
                 o[e] = silu_f(a * sg) * (uu * su);
               } else {
@@ -422,7 +527,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             void* p = sp + swz(row_in_tile, c);
             if constexpr (C::OUT_ELEM == 2) {
               uint32_t w[4];
-              if constexpr (C::kEpi == kEpiResidualPartialRms) {
+              if constexpr (EPI == kEpiResidualPartialRms) {
                 const uint4 rv = *reinterpret_cast<const uint4*>(p);
                 const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
@@ -436,13 +541,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               for (int e = 0; e < 4; ++e) {
                 // statistics of the values actually stored (bf16-rounded)
                 const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
-                if constexpr (C::kEpi == kEpiResidualPartialRms) ss += lo * lo + hi * hi;
+                if constexpr (EPI == kEpiResidualPartialRms) ss += lo * lo + hi * hi;
                 if (ep.amax_out) amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
               }
               *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
             } else {
               float4 v = make_float4(o[0], o[1], o[2], o[3]);
-              if constexpr (C::kEpi == kEpiResidualPartialRms) {
+              if constexpr (EPI == kEpiResidualPartialRms) {
                 const float4 rv = *reinterpret_cast<const float4*>(p);
                 v.x += rv.x;
                 v.y += rv.y;
@@ -455,11 +560,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               *reinterpret_cast<float4*>(p) = v;
             }
           }
-          if constexpr (C::kEpi == kEpiResidualPartialRms) {
+          if constexpr (EPI == kEpiResidualPartialRms) {
             const int gcol = col0 + C::BOX_COLS;  // end column of this box
             if (gcol % kPartialCols == 0 || gcol >= N_out) {
               if (row < M) ep.P[static_cast<int64_t>(row) * ep.T + col0 / kPartialCols] = ss;
               ss = 0.0f;
+              if constexpr (C::TWO_PHASE) __threadfence();  // P visible before the band's release
             }
           }
         }
@@ -467,25 +573,49 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         fence_proxy_async_smem();
         if (!named_bar_and(1, C::NUM_EPI_THREADS, got)) {
           ok = false;
-          break;
+          return;
         }
         if (leader) {
-          tma_store_2d(&tmD, sp, col0, row0);
+          tma_store_2d(mD, sp, col0, row0);
           tma_store_commit();
           tma_store_wait_read_all();  // slot readable again before anyone rewrites it
-          if constexpr (C::kEpi == kEpiResidualPartialRms) mbar_arrive(&r_empty[slot]);
+          if constexpr (C::HAS_LOADER) mbar_arrive(&r_empty[slot]);
         }
         if (++slot == C::NSLOTS) {
           slot = 0;
           sphase ^= 1u;
         }
       }
+      if constexpr (C::TWO_PHASE && EPI == kEpiResidualPartialRms) {
+        // h of this tile is in global memory (and P, fenced above): release the band
+        if (leader) {
+          tma_store_wait_all();
+          fence_proxy_async_global();
+          red_release_gpu_add(&band_ready[tl.m], 1u);
+        }
+      }
+    };
+
+    for (int t = unit; t < num_tiles && ok; t += n_units, ++it) {
+      const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
+      const int buf = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
+      // one decision for all 128 threads, so no thread is left at a barrier
+      if (!named_bar_and(1, C::NUM_EPI_THREADS, mbar_wait(&acc_full[buf], use, abort_flag, &g_status))) break;
+      tc_fence_after_sync();
+      if (C::TWO_PHASE && tl.phase == 1) {
+        if constexpr (C::TWO_PHASE) run_tile(std::integral_constant<int, C::kEpiB>{}, tl, pb, &tmD_b, buf);
+      } else {
+        run_tile(std::integral_constant<int, C::kEpiA>{}, tl, pa, &tmD, buf);
+      }
     }
-    if (ep.amax_out) {
+    if (pa.ep.amax_out || pb.ep.amax_out) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      // non-negative floats order like their bit patterns
-      if (lane == 0) atomicMax(reinterpret_cast<int*>(ep.amax_out), __float_as_int(amax));
+      // non-negative floats order like their bit patterns; one program per
+      // launch has an amax output (two-phase launches have none)
+      float* dst = pa.ep.amax_out ? pa.ep.amax_out : pb.ep.amax_out;
+      if (lane == 0) atomicMax(reinterpret_cast<int*>(dst), __float_as_int(amax));
     }
     if (leader) tma_store_wait_all();
   }
@@ -498,6 +628,19 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if constexpr (C::CG == 2) cluster_sync();
   tc_fence_after_sync();
   if (warp == 1) tmem_dealloc<C::CG>(tmem_base, C::TMEM_COLS);
+  if constexpr (C::TWO_PHASE) {
+    // the last CTA out resets the band counters, so the workspace is zero
+    // again for the next launch
+    if (threadIdx.x == 0) {
+      unsigned* done = band_ready + m_tiles;
+      __threadfence();
+      if (atomicAdd(done, 1u) == gridDim.x - 1) {
+        for (int i = 0; i < m_tiles; ++i) band_ready[i] = 0u;
+        *done = 0u;
+        __threadfence();
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ host ----
@@ -508,18 +651,29 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
                               : C::kKind == kKindTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                                       : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUtensorMapDataType out_dt = C::OUT_ELEM == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUtensorMap tmA, tmB, tmB2, tmR, tmD;
-  const uint64_t kbytes = static_cast<uint64_t>(p.K) * C::ELEM;
-  const uint64_t obytes = static_cast<uint64_t>(p.N_out) * C::OUT_ELEM;
-  CUresult e = encode_tmap_2d(&tmA, in_dt, p.A, p.K, p.M, kbytes, C::BK, C::BM);
-  if (e == CUDA_SUCCESS) e = encode_tmap_2d(&tmB, in_dt, p.B, p.K, p.N_out, kbytes, C::BK, C::B_BOX_ROWS);
+  CUtensorMap tmA, tmB, tmB2, tmR, tmD, tmA_b, tmB_b, tmB2_b, tmD_b;
+  // operand maps of one phase: A [M, K], B (and B2) [N_out, K], output [M, N_out]
+  auto encode_phase = [&](CUtensorMap* a, CUtensorMap* b, CUtensorMap* b2, CUtensorMap* d, const void* A,
+                          const void* B, const void* B2, void* D, int N_out, int K, int epi) {
+    const uint64_t kbytes = static_cast<uint64_t>(K) * C::ELEM;
+    const uint64_t obytes = static_cast<uint64_t>(N_out) * C::OUT_ELEM;
+    const uint32_t brows = static_cast<uint32_t>(C::b_box_rows(epi));
+    CUresult e = encode_tmap_2d(a, in_dt, A, K, p.M, kbytes, C::BK, C::BM);
+    if (e == CUDA_SUCCESS) e = encode_tmap_2d(b, in_dt, B, K, N_out, kbytes, C::BK, brows);
+    if (e == CUDA_SUCCESS) e = encode_tmap_2d(b2, in_dt, B2 ? B2 : B, K, N_out, kbytes, C::BK, brows);
+    if (e == CUDA_SUCCESS) e = encode_tmap_2d(d, out_dt, D, N_out, p.M, obytes, C::BOX_COLS, C::BM);
+    return e;
+  };
+  CUresult e = encode_phase(&tmA, &tmB, &tmB2, &tmD, p.A, p.B, p.B2, p.D, p.N_out, p.K, C::kEpiA);
   if (e == CUDA_SUCCESS)
-    e = encode_tmap_2d(&tmB2, in_dt, C::kEpi == kEpiSwiGLU ? p.B2 : p.B, p.K, p.N_out, kbytes, C::BK,
-                       C::B_BOX_ROWS);
-  if (e == CUDA_SUCCESS)
-    e = encode_tmap_2d(&tmR, out_dt, C::kEpi == kEpiResidualPartialRms ? p.R : p.D, p.N_out, p.M, obytes,
-                       C::BOX_COLS, C::BM);
-  if (e == CUDA_SUCCESS) e = encode_tmap_2d(&tmD, out_dt, p.D, p.N_out, p.M, obytes, C::BOX_COLS, C::BM);
+    e = encode_tmap_2d(&tmR, out_dt, C::HAS_LOADER ? p.R : p.D, p.N_out, p.M,
+                       static_cast<uint64_t>(p.N_out) * C::OUT_ELEM, C::BOX_COLS, C::BM);
+  if (e == CUDA_SUCCESS) {
+    if constexpr (C::TWO_PHASE)
+      e = encode_phase(&tmA_b, &tmB_b, &tmB2_b, &tmD_b, p.b.A, p.b.B, p.b.B2, p.b.D, p.b.N_out, p.b.K, C::kEpiB);
+    else
+      tmA_b = tmA, tmB_b = tmB, tmB2_b = tmB2, tmD_b = tmD;  // unused by a one-phase launch
+  }
   if (e != CUDA_SUCCESS) {
     *msg = "cuTensorMapEncodeTiled rejected an operand (pointer, stride or extent)";
     return cudaErrorInvalidValue;
@@ -565,12 +719,16 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
   }
   const int units = dev < 32 ? max_units[dev] : device_sm_count() / C::CG;
   const int m_tiles = (p.M + C::TILE_M - 1) / C::TILE_M;
-  const int n_tiles = (p.N_out + C::OUT_COLS - 1) / C::OUT_COLS;
-  const int num_tiles = m_tiles * n_tiles;
+  int num_tiles = m_tiles * ((p.N_out + C::out_cols(C::kEpiA) - 1) / C::out_cols(C::kEpiA));
+  if constexpr (C::TWO_PHASE) num_tiles += m_tiles * ((p.b.N_out + C::out_cols(C::kEpiB) - 1) / C::out_cols(C::kEpiB));
+  // a two-phase launch needs every CTA resident (its waits span CTAs): the
+  // grid never exceeds the co-resident units
   const int grid = C::CG * (num_tiles < units ? num_tiles : units);
-  int M = p.M, N = p.N_out, K = p.K;
-  EpiParams ep = p.ep;
-  void* args[] = {&tmA, &tmB, &tmB2, &tmR, &tmD, &M, &N, &K, &ep};
+  int M = p.M;
+  PhaseArgs pa = {p.N_out, p.K, p.ep};
+  PhaseArgs pb = {p.b.N_out, p.b.K, p.b.ep};
+  unsigned* band_ready = p.band_ready;
+  void* args[] = {&tmA, &tmB, &tmB2, &tmR, &tmD, &tmA_b, &tmB_b, &tmB2_b, &tmD_b, &M, &pa, &pb, &band_ready};
   ce = launch_ex(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(C::NUM_THREADS), C::SMEM_BYTES, p.stream,
                  p.pdl, args, C::CG);
   if (ce != cudaSuccess) *msg = "GEMM kernel launch failed";
@@ -592,19 +750,26 @@ inline int choose_cta_group(const GemmProblem& p) {
 // Shared memory per CTA (227 KB max):
 //   one CTA per MMA : 48 KB stages; residual 3 stages + 4 R slots, others 4 + 2
 //   CTA pairs       : 32 KB stages; residual 5 stages + 4 R slots, others 6 + 2
+//   two-phase       : as the residual program (its slot ring serves both phases)
 template <int KIND>
 cudaError_t launch_gemm(const GemmProblem& p, const char** msg) {
   const bool pair = choose_cta_group(p) == 2;
+  if (p.b.epi == kEpiRowScale)
+    return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 5, 4, 2>>(p, msg)
+                : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 3, 4, 1>>(p, msg);
+  if (p.b.epi == kEpiSwiGLU)
+    return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiSwiGLU, 5, 4, 2>>(p, msg)
+                : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiSwiGLU, 3, 4, 1>>(p, msg);
   switch (p.epi) {
     case kEpiResidualPartialRms:
-      return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, 5, 4, 2>>(p, msg)
-                  : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, 3, 4, 1>>(p, msg);
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kNoPhase, 5, 4, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kNoPhase, 3, 4, 1>>(p, msg);
     case kEpiRowScale:
-      return pair ? launch_cfg<GemmCfg<KIND, kEpiRowScale, 6, 2, 2>>(p, msg)
-                  : launch_cfg<GemmCfg<KIND, kEpiRowScale, 4, 2, 1>>(p, msg);
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiRowScale, kNoPhase, 6, 2, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiRowScale, kNoPhase, 4, 2, 1>>(p, msg);
     case kEpiSwiGLU:
-      return pair ? launch_cfg<GemmCfg<KIND, kEpiSwiGLU, 6, 2, 2>>(p, msg)
-                  : launch_cfg<GemmCfg<KIND, kEpiSwiGLU, 4, 2, 1>>(p, msg);
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiSwiGLU, kNoPhase, 6, 2, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiSwiGLU, kNoPhase, 4, 2, 1>>(p, msg);
     default:
       *msg = "unknown epilogue program";
       return cudaErrorInvalidValue;

@@ -176,6 +176,35 @@ CODA_API coda_status coda_gemm_swiglu_fused_rms(const void* H, const void* Wgt, 
                                                 coda_dtype dtype, const float* scale_h, const float* scale_wg,
                                                 const float* scale_wu, float* amax_act, cudaStream_t stream);
 
+/* The whole block in ONE persistent launch: GEMM1 with the residual add and
+ * partial RMS, then the consuming GEMM with the reduction folded into its
+ * epilogue (the single-launch chain that the "very light" reduction of
+ * section "CODA: the treasure hidden in the epilogue" makes possible).  The
+ * consuming GEMM's tiles of a row band start as soon as every GEMM1 tile of
+ * that band has stored h and P, filling the SMs that GEMM1's last wave leaves
+ * idle.  Results equal the separate calls bit for bit.
+ *   coda_block_rowscale:  h = R + X.W1t^T, P, r (r_out, nullable), Z = diag(r) h W2t^T
+ *   coda_block_swiglu:    h, P, r, Act = silu(r h Wgt^T) * (r h Wut^T)
+ *   X [M, K]; W1t [N, K]; R, H [M, N]; P [M, coda_partial_cols(N)] fp32;
+ *   W2t [N2, N] / Wgt, Wut [I, N] (gamma folded in); Z [M, N2] / Act [M, I].
+ *   dtype: CODA_F32 or CODA_BF16 (CODA_E4M3 -> CODA_ERR_UNSUPPORTED: FP8
+ *     quantises h with its per-tensor amax, which needs all of h first).
+ *   workspace: device memory of coda_block_workspace_bytes(M) bytes, zeroed
+ *     by the caller before its first use; every call leaves it zeroed again
+ *     (the last CTA to finish resets it), so it can be reused without a
+ *     memset.  Calls that share a workspace must not overlap on the GPU.
+ *   The grid never exceeds the CTAs that fit on the GPU at once, which the
+ *   band waits require; each wait is bounded and reports CODA_ERR_TIMEOUT
+ *   through coda_get_device_status(). */
+CODA_API int64_t coda_block_workspace_bytes(int64_t M);
+CODA_API coda_status coda_block_rowscale(const void* X, const void* W1t, const void* R, const void* W2t, float eps,
+                                         void* H, float* P, float* r_out, void* Z, int64_t M, int64_t N, int64_t K,
+                                         int64_t N2, coda_dtype dtype, void* workspace, cudaStream_t stream);
+CODA_API coda_status coda_block_swiglu(const void* X, const void* W1t, const void* R, const void* Wgt,
+                                       const void* Wut, float eps, void* H, float* P, float* r_out, void* Act,
+                                       int64_t M, int64_t N, int64_t K, int64_t I, coda_dtype dtype, void* workspace,
+                                       cudaStream_t stream);
+
 /* Per-tensor absolute maximum: *amax = max_i |x_i| over n elements of
  * dtype CODA_F32 or CODA_BF16 (overwritten).  n may be 0 (amax = 0).
  * The FP8 operands of the block's LLaMA-8B workload use per-tensor scales. */

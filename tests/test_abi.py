@@ -104,3 +104,16 @@ def test_binding_fails_loudly_without_cuda_tensors():
     X = torch.zeros(4, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         g.coda_gemm_residual_partial_rms(X, X, X, X, X)
+
+
+def test_block_calls_validate(lib):
+    # FP8 operands are refused (h needs its per-tensor amax first); a missing workspace is an argument error
+    B = A + 512 * MB
+    args = [A, A + 64 * MB, A + 128 * MB, A + 192 * MB, 1e-5, A + 256 * MB, A + 320 * MB, None, A + 384 * MB,
+            256, 512, 512, 512]
+    assert lib.coda_block_rowscale(*args, 2, B, None) == g.CODA_ERR_UNSUPPORTED
+    assert lib.coda_block_rowscale(*args, 1, None, None) == g.CODA_ERR_INVALID_ARG
+    assert b"workspace" in lib.coda_last_error()
+    assert lib.coda_block_rowscale(*args, 1, A + 256 * MB, None) == g.CODA_ERR_INVALID_ARG  # workspace inside h
+    assert lib.coda_block_workspace_bytes(8192) == (64 + 1) * 4
+    assert lib.coda_block_workspace_bytes(1) == 8

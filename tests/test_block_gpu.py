@@ -1,0 +1,90 @@
+"""One-launch blocks (coda_block_rowscale, coda_block_swiglu): the residual
+GEMM and its consumer in one persistent kernel, the consumer's row bands
+waiting on per-band counters.  Every output must equal the separate-call path
+bit for bit, match the oracle, and leave the workspace zeroed for reuse; both
+CTA-group forms; ragged shapes; back-to-back calls on one workspace."""
+import pytest
+import torch
+
+from coda_inputs import WORKLOADS, Workload, make_inputs
+from parity_util import compare, oracle_ref, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gemm_epilogue_fusion_gb300 as g
+    g.load_library()
+    yield
+    g.coda_get_device_status()
+
+
+def run_block(w, d, ws):
+    import gemm_epilogue_fusion_gb300 as g
+    from gemm_epilogue_fusion_gb300 import chain as C
+    gam = {k: d[k] for k in d if k.startswith("gamma")}
+    Wd = {k: d[k] for k in d if k.startswith("W")}
+    f = C.fold_weights(w.chain, Wd, gam)
+    r = torch.empty(w.M, dtype=torch.float32, device="cuda")
+    if w.chain == "rowscale":
+        h, P, Z = g.coda_block_rowscale(d["X"], d["W1t"], d["R"], f["W2t"], w.eps, ws, r_out=r)
+        out = {"h": h, "P": P, "r": r, "Z": Z}
+    else:
+        h, P, act = g.coda_block_swiglu(d["X"], d["W1t"], d["R"], f["Wgt"], f["Wut"], w.eps, ws, r_out=r)
+        out = {"h": h, "P": P, "r": r, "act": act}
+    torch.cuda.synchronize()
+    return {k: v.cpu() for k, v in out.items()}
+
+
+CASES = [
+    WORKLOADS["tiny_f32"],
+    Workload("block_ragged_rowscale", "rowscale", 300, 520, 264, 136, 0, "bf16", 1e-5, 51),
+    Workload("block_ragged_swiglu", "swiglu", 520, 264, 392, 200, 0, "bf16", 1e-5, 52),
+    Workload("block_f32_swiglu", "swiglu", 257, 128, 256, 136, 0, "f32", 1e-5, 53),
+    WORKLOADS["llama1b_attn_out_swiglu"].with_rows(1000),
+    WORKLOADS["llama1b_mlp_down_qkv"].with_rows(777),
+]
+
+
+@pytest.mark.parametrize("cg", ["1", "2"])
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_block_equals_separate_calls(w, cg, monkeypatch):
+    import gemm_epilogue_fusion_gb300 as g
+    monkeypatch.setenv("CODA_CTA_GROUP", cg)
+    inp = make_inputs(w)
+    d = to_device(inp)
+    ws = g.block_workspace(w.M, "cuda")
+    sep = run_gpu(w, d, fused_reduce=True)
+    for _ in range(2):  # the second call reuses the workspace the first left zeroed
+        blk = run_block(w, d, ws)
+        assert torch.count_nonzero(ws).item() == 0, "workspace not left zeroed"
+        for k in blk:
+            assert torch.equal(blk[k], sep[k]), k
+    compare(w, blk, oracle_ref(w, inp))
+
+
+@pytest.mark.parametrize("name", ["llama1b_attn_out_swiglu", "llama1b_mlp_down_qkv"])
+def test_block_full_size_equals_separate_calls(name):
+    import gemm_epilogue_fusion_gb300 as g
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    d = to_device(inp)
+    ws = g.block_workspace(w.M, "cuda")
+    sep = run_gpu(w, d, fused_reduce=True)
+    blk = run_block(w, d, ws)
+    for k in blk:
+        assert torch.equal(blk[k], sep[k]), k
+    assert torch.count_nonzero(ws).item() == 0
+
+
+def test_block_rejects_fp8_and_missing_workspace():
+    import gemm_epilogue_fusion_gb300 as g
+    X = torch.zeros(128, 128, dtype=torch.uint8, device="cuda")
+    W = torch.zeros(128, 128, dtype=torch.uint8, device="cuda")
+    R = torch.zeros(128, 128, dtype=torch.bfloat16, device="cuda")
+    ws = g.block_workspace(128, "cuda")
+    with pytest.raises(g.CodaError, match="UNSUPPORTED"):
+        g.coda_block_rowscale(X, W, R, W, 1e-5, ws, H=R.clone(), Z=R.clone())
