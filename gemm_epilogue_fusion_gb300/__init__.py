@@ -56,6 +56,8 @@ SIGNATURES = {
                                    _vp]),
     "coda_block_swiglu": (_i32, [_vp, _vp, _vp, _vp, _vp, _f32, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _i64, _i32, _vp,
                                  _vp]),
+    "coda_block_swiglu_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _f32, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _i64,
+                                         _i32, _vp]),
     "coda_amax": (_i32, [_vp, _i64, _i32, _fp, _vp]),
     "coda_quantize_e4m3": (_i32, [_vp, _i64, _i32, _fp, _vp, _fp, _vp]),
     "coda_get_device_status": (_i32, []),
@@ -275,6 +277,21 @@ def coda_block_swiglu(X, W1t, R, Wgt, Wut, eps: float, workspace, H=None, P=None
     _check(lib.coda_block_swiglu(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"),
                                  float(eps), _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"), _dev(Act, "Act"), M, N,
                                  K, I, code, _dev(workspace, "workspace"), _stream(X, stream)))
+    return H, P, Act
+
+
+def coda_block_swiglu_noalloc(X, W1t, R, Wgt, Wut, eps: float, H=None, P=None, Act=None, r_out=None, stream=None):
+    """coda_block_swiglu without a workspace, for callers that cannot allocate
+    device memory (the library keeps the counters itself; M <= 131072; calls
+    must not overlap on the GPU).  Returns (h, P, Act)."""
+    lib = load_library()
+    M, K = X.shape
+    N, I = W1t.shape[0], Wgt.shape[0]
+    code = _dtype_code(X)
+    H, P, Act = _block_outputs(X, R, N, I, H, P, Act, code)
+    _check(lib.coda_block_swiglu_noalloc(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(Wgt, "Wgt"),
+                                         _dev(Wut, "Wut"), float(eps), _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"),
+                                         _dev(Act, "Act"), M, N, K, I, code, _stream(X, stream)))
     return H, P, Act
 
 

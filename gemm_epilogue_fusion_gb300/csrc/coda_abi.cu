@@ -18,6 +18,8 @@
 namespace {
 
 thread_local char g_msg[512] = "";
+// Largest M that coda_block_swiglu_noalloc accepts (its counters are built in).
+constexpr int kNoAllocMaxRows = 131072;
 
 coda_status fail(coda_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 coda_status fail(coda_status s, const char* fmt, ...) {
@@ -590,3 +592,57 @@ coda_status coda_get_device_status(void) {
 }
 
 }  // extern "C"
+
+// --------------------------------------------------- allocation-free block ----
+// Some callers cannot call cudaMalloc at all: runtimes that own every byte of
+// device memory and hand a kernel library no workspace, and hot paths where
+// an allocation (which may synchronise the device) is not acceptable.  For
+// them coda_block_swiglu_noalloc keeps the one-launch block's band counters
+// in this file-scope device array instead of a caller workspace.  Every GPU
+// that loads the library holds it (4100 bytes) until the process exits.
+static __device__ __align__(256) unsigned g_noalloc_band_counters[(kNoAllocMaxRows + 127) / 128 + 1];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// The array's name is only a host-side stand-in: the kernel needs its device
+// address, looked up once per device with that device current.
+coda_status noalloc_counters(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(CODA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_band_counters);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(band counters)");
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return CODA_OK;
+}
+
+}  // namespace
+
+extern "C" coda_status coda_block_swiglu_noalloc(const void* X, const void* W1t, const void* R, const void* Wgt,
+                                                 const void* Wut, float eps, void* H, float* P, float* r_out,
+                                                 void* Act, int64_t M, int64_t N, int64_t K, int64_t I,
+                                                 coda_dtype dtype, cudaStream_t stream) {
+  g_msg[0] = 0;
+  if (M > kNoAllocMaxRows)
+    return fail(CODA_ERR_INVALID_ARG,
+                "M = %" PRId64 " exceeds the %d rows of the library's built-in band counters; use coda_block_swiglu "
+                "with a workspace",
+                M, kNoAllocMaxRows);
+  if (M <= 0) return coda_block_swiglu(X, W1t, R, Wgt, Wut, eps, H, P, r_out, Act, M, N, K, I, dtype, nullptr, stream);
+  void* counters = nullptr;
+  TRY(noalloc_counters(&counters));
+  // every call shares the array: start from zero whatever the last call left
+  const int64_t bytes = coda_block_workspace_bytes(M);
+  cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(bytes), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(band counters)");
+  return coda_block_swiglu(X, W1t, R, Wgt, Wut, eps, H, P, r_out, Act, M, N, K, I, dtype, counters, stream);
+}

@@ -205,6 +205,26 @@ CODA_API coda_status coda_block_swiglu(const void* X, const void* W1t, const voi
                                        int64_t M, int64_t N, int64_t K, int64_t I, coda_dtype dtype, void* workspace,
                                        cudaStream_t stream);
 
+/* coda_block_swiglu for callers that cannot allocate device memory (no
+ * counterpart in the CODA write-ups: it exists for the way some programs
+ * manage memory).  Runtimes that own all device memory and give a kernel
+ * library no workspace, and hot paths that must not call cudaMalloc (which
+ * may synchronise the device), can use this form: it takes no workspace and
+ * allocates nothing.  Its band counters live in a fixed array inside the
+ * library (4100 bytes on every GPU that loads it, held until the process
+ * exits).
+ *   Limit: M <= 131072 rows; larger M returns CODA_ERR_INVALID_ARG.
+ *   The first call on a device looks up the array's device address for that
+ *   device (with it current); make that first call before any stream capture.
+ *   Every call shares the one array: each call zeroes the counters it uses
+ *   (an asynchronous memset on `stream`) before its kernel, so calls that
+ *   overlap on the GPU, on any streams, race and must not be issued.
+ *   Other arguments and results as for coda_block_swiglu. */
+CODA_API coda_status coda_block_swiglu_noalloc(const void* X, const void* W1t, const void* R, const void* Wgt,
+                                               const void* Wut, float eps, void* H, float* P, float* r_out,
+                                               void* Act, int64_t M, int64_t N, int64_t K, int64_t I,
+                                               coda_dtype dtype, cudaStream_t stream);
+
 /* Per-tensor absolute maximum: *amax = max_i |x_i| over n elements of
  * dtype CODA_F32 or CODA_BF16 (overwritten).  n may be 0 (amax = 0).
  * The FP8 operands of the block's LLaMA-8B workload use per-tensor scales. */

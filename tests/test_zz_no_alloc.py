@@ -1,0 +1,58 @@
+"""coda_block_swiglu_noalloc: the one-launch SwiGLU block for callers that
+cannot allocate device memory (its band counters live inside the library).
+Called through the C ABI, twice in a row (the second call reuses the built-in
+counters the first one left behind), its outputs must match the workspace
+form coda_block_swiglu within the parity tolerance.  This file runs last, and
+also passes on its own in a fresh process."""
+import os
+import sys
+
+import pytest
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, os.path.dirname(HERE))
+sys.path.insert(0, HERE)
+
+import oracle  # noqa: E402
+from coda_inputs import Workload, make_inputs  # noqa: E402
+
+TOL = 2e-2
+
+
+def _inputs(w):
+    import gemm_epilogue_fusion_gb300 as g
+    inp = make_inputs(w)
+    d = {k: v.cuda() for k, v in inp.items()}
+    Wg = g.coda_fold_gamma(d["Wgt"], d["gamma1"])
+    Wu = g.coda_fold_gamma(d["Wut"], d["gamma1"])
+    return d, Wg, Wu
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("w", [Workload("noalloc_1b", "swiglu", 1000, 2048, 2048, 1024, 0, "bf16", 1e-5, 61),
+                               Workload("noalloc_ragged", "swiglu", 300, 264, 392, 200, 0, "bf16", 1e-5, 62)],
+                         ids=lambda w: w.name)
+def test_noalloc_block_matches_workspace_block_twice(w):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gemm_epilogue_fusion_gb300 as g
+    g.load_library()
+    d, Wg, Wu = _inputs(w)
+    ws = g.block_workspace(w.M, "cuda")
+    h_ref, P_ref, act_ref = g.coda_block_swiglu(d["X"], d["W1t"], d["R"], Wg, Wu, w.eps, ws)
+    for _ in range(2):
+        h, P, act = g.coda_block_swiglu_noalloc(d["X"], d["W1t"], d["R"], Wg, Wu, w.eps)
+        torch.cuda.synchronize()
+        for got, ref in ((h, h_ref), (P, P_ref), (act, act_ref)):
+            assert oracle.rel_err(got.cpu(), ref.cpu()) <= TOL
+    g.coda_get_device_status()
+
+
+def test_noalloc_rejects_rows_beyond_its_counters():
+    import gemm_epilogue_fusion_gb300 as g
+    lib = g.load_library()
+    A = 0x7F0000000000
+    st = lib.coda_block_swiglu_noalloc(A, A, A, A, A, 1e-5, A, A, None, A, 131073, 512, 512, 512, 1, None)
+    assert st == g.CODA_ERR_INVALID_ARG
+    assert b"131072" in lib.coda_last_error()
