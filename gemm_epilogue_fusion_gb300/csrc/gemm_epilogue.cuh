@@ -51,6 +51,18 @@
 
 namespace coda {
 
+// Tuning: rows of one raster band (consecutive tiles walk the band's M-tiles
+// before moving right) and the L2 eviction policy of the A and B operand loads.
+#ifndef CODA_RASTER_ROWS
+#define CODA_RASTER_ROWS 2048
+#endif
+#ifndef CODA_L2_POLICY_A
+#define CODA_L2_POLICY_A l2_policy_evict_last()
+#endif
+#ifndef CODA_L2_POLICY_B
+#define CODA_L2_POLICY_B l2_policy_evict_last()
+#endif
+
 // Per-translation-unit device status word (timeouts), read back and cleared
 // by the TU's read_clear_status_* function.
 namespace {
@@ -93,7 +105,7 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int NUM_EPI_THREADS = 128;
   static constexpr int NUM_THREADS = HAS_LOADER ? 224 : 192;
-  static constexpr int GROUP_M = 16 / CG;  // tile raster: 2048-row bands share each B panel in flight
+  static constexpr int GROUP_M = CODA_RASTER_ROWS / TILE_M;  // tile raster: row bands sharing each B panel
   // shared memory: [A stages][B stages][slots][barriers][tmem slot, abort flag]
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SLOTS = OFF_B + STAGES * B_BYTES;
@@ -287,7 +299,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer ----
     if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_last();
+      const uint64_t pol_a = CODA_L2_POLICY_A, pol_b = CODA_L2_POLICY_B;
       // the stage's completion is counted on the MMA CTA's barrier
       const uint32_t full0 = C::CG == 2 ? mapa_shared(smem_u32(full), 0) : 0u;
       int stage = 0;
@@ -317,22 +329,22 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           uint8_t* b = sB + stage * C::B_BYTES;
           if constexpr (C::CG == 1) {
             mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-            tma_load_2d(a, mA, &full[stage], kx, a_row, pol);
+            tma_load_2d(a, mA, &full[stage], kx, a_row, pol_a);
             if (swiglu) {
-              tma_load_2d(b, mB, &full[stage], kx, tl.n * (C::BN / 2), pol);
-              tma_load_2d(b + (C::BN / 2) * 128, mB2, &full[stage], kx, tl.n * (C::BN / 2), pol);
+              tma_load_2d(b, mB, &full[stage], kx, tl.n * (C::BN / 2), pol_b);
+              tma_load_2d(b + (C::BN / 2) * 128, mB2, &full[stage], kx, tl.n * (C::BN / 2), pol_b);
             } else {
-              tma_load_2d(b, mB, &full[stage], kx, tl.n * C::BN, pol);
+              tma_load_2d(b, mB, &full[stage], kx, tl.n * C::BN, pol_b);
             }
           } else {
             // the MMA CTA expects both CTAs' bytes; the peer only issues its copies
             if (mma_cta) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
             const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
-            tma_load_2d_pair(a, mA, fb, kx, a_row, pol);
+            tma_load_2d_pair(a, mA, fb, kx, a_row, pol_a);
             if (swiglu)  // rank 0: gate rows, rank 1: up rows
-              tma_load_2d_pair(b, cta_rank == 0 ? mB : mB2, fb, kx, tl.n * C::B_ROWS, pol);
+              tma_load_2d_pair(b, cta_rank == 0 ? mB : mB2, fb, kx, tl.n * C::B_ROWS, pol_b);
             else
-              tma_load_2d_pair(b, mB, fb, kx, tl.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS, pol);
+              tma_load_2d_pair(b, mB, fb, kx, tl.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS, pol_b);
           }
           ++issued;
           if (++stage == C::STAGES) {

@@ -74,6 +74,8 @@ def _load():
             lib.coda_oracle_amax.restype = ctypes.c_double
             lib.coda_oracle_e4m3_fake_quant.argtypes = [_dp, _i64, _dp]
             lib.coda_oracle_e4m3_fake_quant.restype = ctypes.c_double
+            lib.coda_oracle_rope.argtypes = [_dp, _i64, _i64, _i64, _i64, ctypes.POINTER(ctypes.c_int64),
+                                             ctypes.c_double]
             _lib = lib
     return _lib
 
@@ -149,6 +151,19 @@ def fake_quant_e4m3(x):
     return out, s
 
 
+def rope(Z, rot_cols: int, head_dim: int, positions, base: float) -> np.ndarray:
+    """RoPE (RoFormer, interleaved pairs) on the first rot_cols columns of Z,
+    head by head; row i rotated for position positions[i].  Returns a copy."""
+    Z = _f64(Z).copy()
+    M, N = Z.shape
+    assert rot_cols <= N and rot_cols % head_dim == 0 and head_dim % 2 == 0
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    assert pos.shape == (M,)
+    _load().coda_oracle_rope(_ptr(Z), M, N, rot_cols, head_dim, pos.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                             float(base))
+    return Z
+
+
 # --------------------------------------------------------------- blocks ----
 
 def block_rowscale(X, W1, R, gamma, W2, eps):
@@ -165,6 +180,14 @@ def block_swiglu(X, W1, R, gamma, Wg, Wu, eps):
     return {"h": h, "r": rstd, "act": swiglu(y, Wg, Wu)}
 
 
+def block_rowscale_rope(X, W1, R, gamma, W2, eps, rot_cols, head_dim, positions, base):
+    """GEMM -> residual add -> RMSNorm -> QKV GEMM -> RoPE on the Q and K
+    columns (the first rot_cols), unfused."""
+    out = block_rowscale(X, W1, R, gamma, W2, eps)
+    out["Z"] = rope(out["Z"], rot_cols, head_dim, positions, base)
+    return out
+
+
 def chain_full(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps):
     """Pre-norm LLaMA block tail and the next layer's QKV projection:
     h1 = R + X.Wo ; y1 = RMSNorm(h1) ; act = SwiGLU(y1) ; h2 = h1 + act.Wd ;
@@ -177,12 +200,16 @@ def chain_full(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps):
     return {"h1": h1, "r1": r1, "act": act, "h2": h2, "r2": r2, "Z": gemm(y2, Wq)}
 
 
-def chain_full_fp8(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps):
+def chain_full_fp8(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps, out_rows=None):
     """Quantisation-aware FP8 chain.  FP8 changes the arithmetic, so here the
     oracle follows the reparameterised steps and quantises exactly the GEMM
     operands an FP8 implementation feeds the tensor cores: X, every weight
     (gamma folded in first), h1, act and h2, each with its own per-tensor
-    scale amax/448.  R, h, r and the outputs stay unquantised."""
+    scale amax/448.  R, h, r and the outputs stay unquantised.
+
+    ``out_rows``: when given, every result is returned for those rows only and
+    the last GEMM (Z) is computed for them alone.  The per-tensor scales still
+    come from the whole tensors, so the values equal the full computation's."""
     q = lambda t: fake_quant_e4m3(t)[0]
     g1, g2 = _f64(gamma1), _f64(gamma2)
     Wg_f = _f64(Wg) * g1[:, None]
@@ -194,10 +221,13 @@ def chain_full_fp8(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps):
     G = gemm(h1q, q(Wg_f)) * r1[:, None]
     U = gemm(h1q, q(Wu_f)) * r1[:, None]
     act = silu_mul(G, U)
+    del G, U
     h2 = gemm(q(act), q(Wd), h1)
     _, r2 = rmsnorm(h2, g2, eps)
-    Z = gemm(q(h2), q(Wq_f)) * r2[:, None]
-    return {"h1": h1, "r1": r1, "act": act, "h2": h2, "r2": r2, "Z": Z}
+    h2q = q(h2)
+    sel = slice(None) if out_rows is None else np.asarray(out_rows)
+    Z = gemm(h2q[sel], q(Wq_f)) * r2[sel][:, None]
+    return {"h1": h1[sel], "r1": r1[sel], "act": act[sel], "h2": h2[sel], "r2": r2[sel], "Z": Z}
 
 
 def rel_err(got, ref) -> float:

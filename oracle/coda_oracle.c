@@ -141,3 +141,27 @@ double coda_oracle_e4m3_fake_quant(const double *x, int64_t n, double *out)
         out[i] = coda_oracle_e4m3_decode(coda_oracle_e4m3_encode(x[i] / s)) * s;
     return s;
 }
+
+/* Rotary position embedding, the RoFormer definition with interleaved pairs
+ * (the CODA write-up names RoPE among the operations that move into a GEMM
+ * epilogue).  For row i at position pos[i], each head of `head_dim` columns
+ * among the first `rot_cols` columns, and pair j < head_dim/2:
+ *   phi = pos[i] * base^(-2j/head_dim)
+ *   (z_2j, z_2j+1) -> (z_2j cos(phi) - z_2j+1 sin(phi), z_2j sin(phi) + z_2j+1 cos(phi))
+ * Columns from rot_cols on (V in a fused QKV output) are left unchanged.
+ * In place on Z [M x N]. */
+void coda_oracle_rope(double *Z, int64_t M, int64_t N, int64_t rot_cols, int64_t head_dim,
+                      const int64_t *pos, double base)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        double *z = Z + i * N;
+        for (int64_t c = 0; c + 1 < rot_cols; c += 2) {
+            const int64_t j = (c % head_dim) / 2;
+            const double phi = (double)pos[i] * pow(base, -2.0 * (double)j / (double)head_dim);
+            const double a = z[c], b = z[c + 1];
+            z[c] = a * cos(phi) - b * sin(phi);
+            z[c + 1] = a * sin(phi) + b * cos(phi);
+        }
+    }
+}

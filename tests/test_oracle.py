@@ -189,3 +189,79 @@ def test_fp8_chain_close_to_exact_chain():
 def test_rel_err_metric():
     assert oracle.rel_err([1.0, 2.0], [1.0, 2.0]) == 0.0
     assert oracle.rel_err([1.0, 2.5], [1.0, 2.0]) == pytest.approx(0.25, rel=1e-6)
+
+
+def test_fp8_chain_row_subset_equals_full_chain():
+    """out_rows only narrows what is returned and which rows the last GEMM
+    computes; the per-tensor scales still come from every row."""
+    rng = np.random.default_rng(7)
+    M, H, I, Q = 20, 32, 48, 24
+    X, Wo, R = rng.standard_normal((M, H)), rng.standard_normal((H, H)), rng.standard_normal((M, H))
+    X[5] *= 50.0  # a heavy row sets the scales; it is not among the returned rows
+    Wg, Wu = rng.standard_normal((H, I)), rng.standard_normal((H, I))
+    Wd, Wq = rng.standard_normal((I, H)), rng.standard_normal((H, Q))
+    g1, g2 = 1 + 0.1 * rng.standard_normal(H), 1 + 0.1 * rng.standard_normal(H)
+    full = oracle.chain_full_fp8(X, Wo, R, g1, Wg, Wu, Wd, g2, Wq, 1e-5)
+    rows = [3, 7, 19]
+    sub = oracle.chain_full_fp8(X, Wo, R, g1, Wg, Wu, Wd, g2, Wq, 1e-5, out_rows=rows)
+    for k in full:
+        np.testing.assert_array_equal(sub[k], full[k][rows])
+
+
+# ----------------------------------------------------------------- RoPE ----
+# RoFormer's rotary embedding in its complex form: viewing pair j of a head as
+# x_2j + i x_2j+1, position p multiplies it by exp(i p base^(-2j/d)).  The
+# oracle writes it as a real rotation; these pins hold it to the complex
+# definition and to the properties that make it a position encoding.
+
+def _rope_complex(Z, rot_cols, d, pos, base):
+    Z = np.array(Z, dtype=np.float64)
+    zc = Z[:, :rot_cols:2] + 1j * Z[:, 1:rot_cols:2]          # [M, rot_cols/2]
+    j = np.arange(rot_cols // 2) % (d // 2)                    # pair index within its head
+    zc = zc * np.exp(1j * np.outer(pos, base ** (-2.0 * j / d)))
+    Z[:, :rot_cols:2], Z[:, 1:rot_cols:2] = zc.real, zc.imag
+    return Z
+
+
+def test_rope_matches_complex_multiplication_and_leaves_v():
+    rng = np.random.default_rng(8)
+    M, N, rot, d = 9, 48, 32, 8
+    Z = rng.standard_normal((M, N))
+    pos = rng.integers(0, 5000, M)
+    got = oracle.rope(Z, rot, d, pos, 500000.0)
+    np.testing.assert_allclose(got, _rope_complex(Z, rot, d, pos, 500000.0), rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(got[:, rot:], Z[:, rot:])
+
+
+def test_rope_position_zero_is_identity_and_positions_compose():
+    rng = np.random.default_rng(9)
+    Z = rng.standard_normal((4, 16))
+    np.testing.assert_array_equal(oracle.rope(Z, 16, 8, np.zeros(4), 10000.0), Z)
+    p1, p2 = np.array([1, 7, 100, 2047]), np.array([3, 0, 900, 1])
+    twice = oracle.rope(oracle.rope(Z, 16, 8, p1, 10000.0), 16, 8, p2, 10000.0)
+    np.testing.assert_allclose(twice, oracle.rope(Z, 16, 8, p1 + p2, 10000.0), rtol=1e-10, atol=1e-12)
+
+
+def test_rope_first_pair_turns_by_the_position_in_every_head():
+    # theta_0 = base^0 = 1 whatever the base, and the frequency index restarts
+    # in each head: column 0 and column d of (1, 0, ...) rotate by exactly p
+    d = 4
+    Z = np.zeros((1, 8))
+    Z[0, 0] = Z[0, d] = 1.0
+    got = oracle.rope(Z, 8, d, np.array([1]), 123.0)
+    for c in (0, d):
+        assert got[0, c] == pytest.approx(math.cos(1.0), abs=1e-15)
+        assert got[0, c + 1] == pytest.approx(math.sin(1.0), abs=1e-15)   # counter-clockwise
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    rng = np.random.default_rng(10)
+    d = 16
+    q, k = rng.standard_normal((1, d)), rng.standard_normal((1, d))
+    def score(m, n):
+        return float((oracle.rope(q, d, d, np.array([m]), 500000.0) @ oracle.rope(k, d, d, np.array([n]), 500000.0).T)[0, 0])
+    assert score(10, 3) == pytest.approx(score(1010, 1003), rel=1e-9)
+    assert score(5, 5) == pytest.approx(float((q @ k.T)[0, 0]), rel=1e-12)
+    # and each pair keeps its length
+    z = oracle.rope(q, d, d, np.array([777]), 500000.0)
+    np.testing.assert_allclose(z[0, ::2] ** 2 + z[0, 1::2] ** 2, q[0, ::2] ** 2 + q[0, 1::2] ** 2, rtol=1e-12)
