@@ -44,21 +44,21 @@ def golden_rows(inp, M):
     return sorted(set(sample_rows(M, 6).tolist()) | set(heavy))
 
 
-def main(out=OUT):
+def main(path=OUT):
     w = WORKLOADS["llama8b_chain_fp8"]
     t0 = time.time()
     inp = make_inputs(w)
     rows = golden_rows(inp, w.M)
     T = lambda t: t.double().numpy().T.copy()  # noqa: E731
-    out = oracle.chain_full_fp8(inp["X"], T(inp["W1t"]), inp["R"], inp["gamma1"], T(inp["Wgt"]), T(inp["Wut"]),
+    res = oracle.chain_full_fp8(inp["X"], T(inp["W1t"]), inp["R"], inp["gamma1"], T(inp["Wgt"]), T(inp["Wut"]),
                                 T(inp["Wdt"]), inp["gamma2"], T(inp["Wqt"]), w.eps, out_rows=rows)
-    save = {k: np.asarray(out[k]).astype(np.float32) for k in ("h1", "r1", "act", "h2", "r2", "Z")}
+    save = {k: np.asarray(res[k]).astype(np.float32) for k in ("h1", "r1", "act", "h2", "r2", "Z")}
     dig = input_digests(inp)
-    np.savez_compressed(out, rows=np.asarray(rows, dtype=np.int64),
+    np.savez_compressed(path, rows=np.asarray(rows, dtype=np.int64),
                         digests=np.asarray([f"{k}:{dig[k]}" for k in KEYS]), **save)
     import platform
     import torch
-    print(f"wrote {out} for rows {rows} in {time.time() - t0:.0f} s on {platform.machine()}, torch {torch.__version__}")
+    print(f"wrote {path} for rows {rows} in {time.time() - t0:.0f} s on {platform.machine()}, torch {torch.__version__}")
 
 
 if __name__ == "__main__":
