@@ -480,6 +480,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
       }
       const float sg = rs * sab, su = rs * sab2;
+      // row-scale program with RoPE: this row's cos/sin table row
+      const float4* rope_row = nullptr;
+      if constexpr (EPI == kEpiRowScale) {
+        if (ep.rope_cs != nullptr && row < M) {
+          int pos = ep.rope_pos != nullptr ? ep.rope_pos[row] : row % ep.rope_npos;
+          pos = min(max(pos, 0), ep.rope_npos - 1);  // out-of-range positions are clamped
+          rope_row = reinterpret_cast<const float4*>(ep.rope_cs + 2 * static_cast<int64_t>(pos) * ep.rope_half);
+        }
+      }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::BN);
       auto release_acc = [&]() {
         // last TMEM read of this tile: hand the accumulator back to the MMA warp
@@ -534,6 +543,23 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 o[e] = silu_f(a * sg) * (uu * su);
               } else {
                 o[e] = a * sg;
+              }
+            }
+            if constexpr (EPI == kEpiRowScale) {
+              const int col = col0 + c * C::CHUNK_COLS;
+              if (rope_row != nullptr && col < ep.rope_cols) {
+                // RoPE on interleaved pairs; the chunk's CHUNK_COLS / 2 pairs are
+                // consecutive frequencies of one head (head_dim % CHUNK_COLS == 0)
+                const int j0 = (col >> 1) % ep.rope_half;
+#pragma unroll
+                for (int e2 = 0; e2 < C::CHUNK_COLS / 4; ++e2) {
+                  const float4 cs = __ldg(rope_row + (j0 >> 1) + e2);  // cos_j, sin_j, cos_j+1, sin_j+1
+                  const float x0 = o[4 * e2], y0 = o[4 * e2 + 1], x1 = o[4 * e2 + 2], y1 = o[4 * e2 + 3];
+                  o[4 * e2] = x0 * cs.x - y0 * cs.y;
+                  o[4 * e2 + 1] = x0 * cs.y + y0 * cs.x;
+                  o[4 * e2 + 2] = x1 * cs.z - y1 * cs.w;
+                  o[4 * e2 + 3] = x1 * cs.w + y1 * cs.z;
+                }
               }
             }
             void* p = sp + swz(row_in_tile, c);
