@@ -58,9 +58,8 @@ SIGNATURES = {
                                  _vp]),
     "coda_block_swiglu_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _f32, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _i64,
                                          _i32, _vp]),
-    "coda_rope_table": (_i32, [_fp, _i64, _i64, ctypes.c_double, _vp]),
-    "coda_gemm_rowscale_rope": (_i32, [_vp, _vp, _fp, _fp, _f32, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _fp,
-                                       _i64, _i64, _i64, _vp, _vp]),
+    "coda_gemm_rowscale_rope": (_i32, [_vp, _vp, _fp, _fp, _f32, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _i64,
+                                       _i64, ctypes.c_double, _i64, _vp, _vp]),
     "coda_amax": (_i32, [_vp, _i64, _i32, _fp, _vp]),
     "coda_quantize_e4m3": (_i32, [_vp, _i64, _i32, _fp, _vp, _fp, _vp]),
     "coda_get_device_status": (_i32, []),
@@ -235,18 +234,11 @@ def coda_gemm_swiglu_fused_rms(H, Wgt, Wut, P, eps: float, Act=None, r_out=None,
     return Act
 
 
-def coda_rope_table(n_pos: int, head_dim: int, base: float, device="cuda", out=None, stream=None):
-    """cos/sin table [n_pos, head_dim/2, 2] fp32 of RoPE angles p * base^(-2j/head_dim)."""
-    lib = load_library()
-    if out is None:
-        out = torch.empty(n_pos, head_dim // 2, 2, dtype=torch.float32, device=device)
-    _check(lib.coda_rope_table(_dev(out, "cos_sin"), n_pos, head_dim, float(base), _stream(out, stream)))
-    return out
-
-
-def coda_gemm_rowscale_rope(H, W2t, cos_sin, head_dim: int, rope_cols: int, *, r=None, P=None, eps: float = 0.0,
-                            r_out=None, positions=None, Z=None, scale_h=None, scale_w=None, stream=None):
-    """Z = RoPE(diag(r) H W2) on the first rope_cols columns; r given, or reduced from P inside the epilogue."""
+def coda_gemm_rowscale_rope(H, W2t, head_dim: int, rope_cols: int, base: float, *, seq_len: int = 0, positions=None,
+                            r=None, P=None, eps: float = 0.0, r_out=None, Z=None, scale_h=None, scale_w=None,
+                            stream=None):
+    """Z = RoPE(diag(r) H W2) on the first rope_cols columns; r given, or reduced from P inside the epilogue.
+    Positions: ``positions`` [M] int32, else row mod ``seq_len``."""
     lib = load_library()
     M, K = H.shape
     N2 = W2t.shape[0]
@@ -255,8 +247,8 @@ def coda_gemm_rowscale_rope(H, W2t, cos_sin, head_dim: int, rope_cols: int, *, r
         Z = torch.empty(M, N2, dtype=_out_dtype(code), device=H.device)
     _check(lib.coda_gemm_rowscale_rope(_dev(H, "H"), _dev(W2t, "W2t"), _dev(r, "r"), _dev(P, "P"), float(eps),
                                        _dev(r_out, "r_out"), _dev(Z, "Z"), M, N2, K, code, _dev(scale_h, "scale_h"),
-                                       _dev(scale_w, "scale_w"), _dev(cos_sin, "cos_sin"), cos_sin.shape[0], head_dim,
-                                       rope_cols, _dev(positions, "positions"), _stream(H, stream)))
+                                       _dev(scale_w, "scale_w"), head_dim, rope_cols, float(base), seq_len,
+                                       _dev(positions, "positions"), _stream(H, stream)))
     return Z
 
 

@@ -314,8 +314,9 @@ namespace {
 
 // RoPE arguments of the row-scale program.
 struct RopeArgs {
-  const float* cos_sin;
-  int64_t n_pos, head_dim, rope_cols;
+  int64_t head_dim, rope_cols;
+  double base;
+  int64_t seq_len;
   const int32_t* positions;
 };
 
@@ -328,16 +329,14 @@ coda_status gemm_rowscale_impl(const void* H, const void* W2t, const float* r, c
   g_msg[0] = 0;
   if (rope) {
     const int64_t chunk = 16 / out_bytes(dtype);  // columns per 16-byte store chunk
-    REQUIRE(rope->n_pos > 0 && rope->n_pos < INT32_MAX, "n_pos out of range");
     REQUIRE(rope->head_dim > 0 && rope->head_dim % chunk == 0,
             "head_dim must be a positive multiple of %" PRId64 " for this dtype", chunk);
     REQUIRE(rope->rope_cols >= 0 && rope->rope_cols <= N2 && rope->rope_cols % rope->head_dim == 0,
             "rope_cols must be a multiple of head_dim within [0, N2]");
-    REQUIRE(rope->n_pos * (rope->head_dim / 2) < INT32_MAX, "cos/sin table too large");
-    if (M > 0) {
-      TRY(check_ptr(rope->cos_sin, "cos_sin"));
-      if (rope->positions) TRY(check_scalar_ptr(rope->positions, "positions"));
-    }
+    REQUIRE(std::isfinite(rope->base) && rope->base > 1.0, "base must be finite and > 1");
+    REQUIRE(rope->positions != nullptr || (rope->seq_len > 0 && rope->seq_len < INT32_MAX),
+            "seq_len must be in [1, 2^31) when positions is NULL");
+    if (M > 0 && rope->positions) TRY(check_scalar_ptr(rope->positions, "positions"));
   }
   TRY(check_gemm_dims(M, N2, K, dtype, "N2"));
   TRY(check_scales(dtype, scale_h, "scale_h", scale_w, "scale_w"));
@@ -358,9 +357,8 @@ coda_status gemm_rowscale_impl(const void* H, const void* W2t, const float* r, c
   const Range ins[] = {rng("H", H, M * K * ib), rng("W2t", W2t, N2 * K * ib), rng("r", r, r ? M * 4 : 0),
                        rng("P", P, P ? M * T * 4 : 0), rng("scale_h", scale_h, scale_h ? 4 : 0),
                        rng("scale_w", scale_w, scale_w ? 4 : 0),
-                       rng("cos_sin", rope ? rope->cos_sin : nullptr, rope ? rope->n_pos * rope->head_dim * 4 : 0),
                        rng("positions", rope ? rope->positions : nullptr, rope && rope->positions ? M * 4 : 0)};
-  TRY(check_overlaps(outs, 2, ins, 8));
+  TRY(check_overlaps(outs, 2, ins, 7));
   coda::GemmProblem p = {};
   p.epi = coda::kEpiRowScale;
   p.A = H;
@@ -378,11 +376,11 @@ coda_status gemm_rowscale_impl(const void* H, const void* W2t, const float* r, c
   p.ep.scale_a = scale_h;
   p.ep.scale_b = scale_w;
   if (rope && rope->rope_cols > 0) {
-    p.ep.rope_cs = rope->cos_sin;
     p.ep.rope_pos = rope->positions;
-    p.ep.rope_npos = static_cast<int>(rope->n_pos);
+    p.ep.rope_seq = static_cast<int>(rope->positions ? 1 : rope->seq_len);
     p.ep.rope_half = static_cast<int>(rope->head_dim / 2);
     p.ep.rope_cols = static_cast<int>(rope->rope_cols);
+    p.ep.rope_log2b = static_cast<float>(std::log2(rope->base) / static_cast<double>(rope->head_dim / 2));
   }
   p.stream = stream;
   p.pdl = use_pdl();
@@ -472,26 +470,15 @@ coda_status coda_gemm_rowscale_fused_rms(const void* H, const void* W2t, const f
   return gemm_rowscale_impl(H, W2t, nullptr, P, eps, r_out, Z, M, N2, K, dtype, scale_h, scale_w, stream);
 }
 
-coda_status coda_rope_table(float* cos_sin, int64_t n_pos, int64_t head_dim, double base, cudaStream_t stream) {
-  g_msg[0] = 0;
-  REQUIRE(n_pos > 0 && head_dim > 0 && head_dim % 2 == 0, "n_pos > 0 and an even head_dim > 0 are required");
-  REQUIRE(n_pos * (head_dim / 2) < INT32_MAX, "cos/sin table too large");
-  REQUIRE(std::isfinite(base) && base > 1.0, "base must be finite and > 1");
-  TRY(check_ptr(cos_sin, "cos_sin"));
-  cudaError_t e = coda::launch_rope_table(cos_sin, n_pos, head_dim / 2, base, stream);
-  return e == cudaSuccess ? CODA_OK : cuda_fail(e, "coda_rope_table launch");
-}
-
 coda_status coda_gemm_rowscale_rope(const void* H, const void* W2t, const float* r, const float* P, float eps,
                                     float* r_out, void* Z, int64_t M, int64_t N2, int64_t K, coda_dtype dtype,
-                                    const float* scale_h, const float* scale_w, const float* cos_sin, int64_t n_pos,
-                                    int64_t head_dim, int64_t rope_cols, const int32_t* positions,
-                                    cudaStream_t stream) {
+                                    const float* scale_h, const float* scale_w, int64_t head_dim, int64_t rope_cols,
+                                    double base, int64_t seq_len, const int32_t* positions, cudaStream_t stream) {
   if (M > 0 && (r == nullptr) == (P == nullptr)) {
     g_msg[0] = 0;
     return fail(CODA_ERR_INVALID_ARG, "exactly one of r and P must be given");
   }
-  const RopeArgs rope = {cos_sin, n_pos, head_dim, rope_cols, positions};
+  const RopeArgs rope = {head_dim, rope_cols, base, seq_len, positions};
   return gemm_rowscale_impl(H, W2t, P ? nullptr : r, P, eps, P ? r_out : nullptr, Z, M, N2, K, dtype, scale_h,
                             scale_w, stream, &rope);
 }

@@ -169,20 +169,6 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   }
 }
 
-// cos/sin table of RoPE: cs[p, j] = (cos phi, sin phi), phi = p * base^(-j / half)
-// (= base^(-2j / head_dim)), evaluated in double precision and stored as fp32.
-__global__ void __launch_bounds__(256) rope_table_kernel(float2* __restrict__ cs, int64_t n, int64_t half,
-                                                         double base) {
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t p = i / half, j = i % half;
-    const double phi = static_cast<double>(p) * pow(base, -static_cast<double>(j) / static_cast<double>(half));
-    double sn, cn;
-    sincos(phi, &sn, &cn);
-    cs[i] = make_float2(static_cast<float>(cn), static_cast<float>(sn));
-  }
-}
-
 int grid_for(int64_t work_items, int threads) {
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
   int64_t g = (work_items + threads - 1) / threads;
@@ -211,12 +197,6 @@ cudaError_t launch_fold_gamma(const void* Wt, const float* gamma, void* Wt_out, 
   else
     fold_gamma_kernel<false><<<g, 256, 0, s>>>(static_cast<const uint4*>(Wt), gamma, static_cast<uint4*>(Wt_out),
                                                n_vec, K);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_rope_table(float* cs, int64_t n_pos, int64_t half, double base, cudaStream_t s) {
-  const int64_t n = n_pos * half;
-  rope_table_kernel<<<grid_for(n, 256), 256, 0, s>>>(reinterpret_cast<float2*>(cs), n, half, base);
   return cudaGetLastError();
 }
 

@@ -47,10 +47,10 @@ struct EpiParams {
   const float* scale_b;   // ... of B (SwiGLU: of the gate weight)
   const float* scale_b2;  // SwiGLU: of the up weight
   float* amax_out;        // nullable: max |stored output|, combined with atomicMax (caller zeroes it)
-  // row-scale program only: RoPE on the first rope_cols output columns
-  const float* rope_cs;   // [rope_npos, rope_half, 2] cos, sin; null = no RoPE
-  const int* rope_pos;    // [M] positions; null = row % rope_npos
-  int rope_npos, rope_half, rope_cols;
+  // row-scale program only: RoPE on the first rope_cols output columns (0 = none)
+  const int* rope_pos;    // [M] positions; null = row % rope_seq
+  int rope_seq, rope_half, rope_cols;
+  float rope_log2b;       // log2(base) / rope_half
 };
 
 // Second phase of a two-phase launch (the consuming GEMM of the block).
@@ -94,7 +94,6 @@ cudaError_t launch_rms_reduce(const float* P, int64_t M, int T, int64_t N, float
                               cudaStream_t s, bool pdl);
 cudaError_t launch_fold_gamma(const void* Wt, const float* gamma, void* Wt_out, int64_t N_out, int64_t K,
                               bool f32, cudaStream_t s);
-cudaError_t launch_rope_table(float* cs, int64_t n_pos, int64_t half, double base, cudaStream_t s);
 cudaError_t launch_amax(const void* x, int64_t n, bool f32, float* amax, cudaStream_t s);
 cudaError_t launch_quantize_e4m3(const void* x, int64_t n, bool f32, const float* amax, uint8_t* q,
                                  float* scale, cudaStream_t s);

@@ -168,6 +168,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// sin and cos of the RoPE angle phi = p * base^(-j / half), with log2b =
+// log2(base) / half.  phi is reduced by whole turns with 2*pi split into a
+// float head and its remainder (Cody and Waite's two-constant reduction), so
+// the fast sincos sees |x| <= pi; the error is dominated by the fp32 product
+// p * inv_freq (about 1.2e-7 * phi radians).
+__device__ __forceinline__ void rope_sincos(float p, int j, float log2b, float& sn, float& cn) {
+  constexpr float kTwoPiHi = 6.28318548202514648f;    // 2*pi rounded to float (above 2*pi)
+  constexpr float kTwoPiLo = -1.74845553146951832e-7f;  // 2*pi - kTwoPiHi
+  const float phi = p * exp2f(-static_cast<float>(j) * log2b);
+  const float k = rintf(phi * 0.159154943091895336f);  // whole turns
+  const float x = fmaf(-k, kTwoPiLo, fmaf(-k, kTwoPiHi, phi));
+  __sincosf(x, &sn, &cn);
+}
+
 // Byte offset of 16-byte chunk `c` (0..7) of row `row` inside one 128B-swizzled
 // box of 128 rows x 128 B: the chunk index is XORed with the row's position in
 // its 8-row atom, as TMA lays it out.
@@ -480,13 +494,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
       }
       const float sg = rs * sab, su = rs * sab2;
-      // row-scale program with RoPE: this row's cos/sin table row
-      const float4* rope_row = nullptr;
+      // row-scale program with RoPE: this row's position
+      bool rope_on = false;
+      float rope_p = 0.0f;
       if constexpr (EPI == kEpiRowScale) {
-        if (ep.rope_cs != nullptr && row < M) {
-          int pos = ep.rope_pos != nullptr ? ep.rope_pos[row] : row % ep.rope_npos;
-          pos = min(max(pos, 0), ep.rope_npos - 1);  // out-of-range positions are clamped
-          rope_row = reinterpret_cast<const float4*>(ep.rope_cs + 2 * static_cast<int64_t>(pos) * ep.rope_half);
+        if (ep.rope_cols > 0 && row < M) {
+          rope_on = true;
+          rope_p = static_cast<float>(ep.rope_pos != nullptr ? ep.rope_pos[row] : row % ep.rope_seq);
         }
       }
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::BN);
@@ -547,18 +561,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             if constexpr (EPI == kEpiRowScale) {
               const int col = col0 + c * C::CHUNK_COLS;
-              if (rope_row != nullptr && col < ep.rope_cols) {
+              if (rope_on && col < ep.rope_cols) {
                 // RoPE on interleaved pairs; the chunk's CHUNK_COLS / 2 pairs are
-                // consecutive frequencies of one head (head_dim % CHUNK_COLS == 0)
+                // consecutive frequencies j of one head (head_dim % CHUNK_COLS == 0)
                 const int j0 = (col >> 1) % ep.rope_half;
 #pragma unroll
-                for (int e2 = 0; e2 < C::CHUNK_COLS / 4; ++e2) {
-                  const float4 cs = __ldg(rope_row + (j0 >> 1) + e2);  // cos_j, sin_j, cos_j+1, sin_j+1
-                  const float x0 = o[4 * e2], y0 = o[4 * e2 + 1], x1 = o[4 * e2 + 2], y1 = o[4 * e2 + 3];
-                  o[4 * e2] = x0 * cs.x - y0 * cs.y;
-                  o[4 * e2 + 1] = x0 * cs.y + y0 * cs.x;
-                  o[4 * e2 + 2] = x1 * cs.z - y1 * cs.w;
-                  o[4 * e2 + 3] = x1 * cs.w + y1 * cs.z;
+                for (int e = 0; e < C::CHUNK_COLS / 2; ++e) {
+                  float sn, cn;
+                  rope_sincos(rope_p, j0 + e, ep.rope_log2b, sn, cn);
+                  const float x = o[2 * e], y = o[2 * e + 1];
+                  o[2 * e] = x * cn - y * sn;
+                  o[2 * e + 1] = x * sn + y * cn;
                 }
               }
             }

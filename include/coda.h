@@ -149,25 +149,20 @@ CODA_API coda_status coda_gemm_rowscale(const void* H, const void* W2t, const fl
  *   phi = p_i * base^(-2j / head_dim)
  *   (z_2j, z_2j+1) <- (z_2j cos phi - z_2j+1 sin phi, z_2j sin phi + z_2j+1 cos phi)
  * applied in fp32 to Z = r * (H . W2t^T) before the single rounding to the
- * output type.
+ * output type.  The angle is formed in fp32 and reduced by whole turns, so its
+ * error is about 1.2e-7 * phi radians (2.4e-4 at phi = 2047).
  *
- * coda_rope_table fills cos_sin [n_pos, head_dim/2, 2] fp32 with (cos phi,
- * sin phi) for positions 0..n_pos-1 (evaluated in double precision), once
- * per (n_pos, head_dim, base); base finite and > 1, head_dim even.
- *
- * coda_gemm_rowscale_rope: as coda_gemm_rowscale (r given) or
- * coda_gemm_rowscale_fused_rms (P and eps given, r_out nullable): exactly one
- * of r and P.  positions [M] int32 (nullable: p_i = i mod n_pos, rows laid
- * out batch-major); positions outside [0, n_pos) are clamped.  head_dim must
- * be a multiple of 8 (bf16, e4m3 operands) or 4 (fp32); rope_cols a multiple
- * of head_dim, at most N2.  cos_sin 16-byte aligned. */
-CODA_API coda_status coda_rope_table(float* cos_sin, int64_t n_pos, int64_t head_dim, double base,
-                                     cudaStream_t stream);
+ * As coda_gemm_rowscale (r given) or coda_gemm_rowscale_fused_rms (P and eps
+ * given, r_out nullable): exactly one of r and P.
+ *   head_dim: a multiple of 8 (bf16, e4m3 operands) or 4 (fp32);
+ *   rope_cols: a multiple of head_dim, at most N2 (0 = no rotation);
+ *   base: finite, > 1 (500000 for LLaMA-3);
+ *   positions: [M] int32, or NULL for p_i = i mod seq_len (rows batch-major). */
 CODA_API coda_status coda_gemm_rowscale_rope(const void* H, const void* W2t, const float* r, const float* P,
                                              float eps, float* r_out, void* Z, int64_t M, int64_t N2, int64_t K,
                                              coda_dtype dtype, const float* scale_h, const float* scale_w,
-                                             const float* cos_sin, int64_t n_pos, int64_t head_dim,
-                                             int64_t rope_cols, const int32_t* positions, cudaStream_t stream);
+                                             int64_t head_dim, int64_t rope_cols, double base, int64_t seq_len,
+                                             const int32_t* positions, cudaStream_t stream);
 
 /* Gate/up GEMM with SwiGLU (and the row scale) in its epilogue:
  *   G = r . (H . Wgt^T),  U = r . (H . Wut^T)   (row scale applied to both

@@ -27,14 +27,14 @@ def run(w, inp, head_dim, rope_cols, n_pos, base, positions=None, fused=True, ro
     d = to_device(inp)
     W2 = g.coda_fold_gamma(d["W2t"], d["gamma1"])
     h, P = g.coda_gemm_residual_partial_rms(d["X"], d["W1t"], d["R"])
-    cs = g.coda_rope_table(n_pos, head_dim, base)
     pos_d = None if positions is None else torch.as_tensor(positions, dtype=torch.int32).cuda()
+    kw = dict(seq_len=n_pos, positions=pos_d)
     if fused:
         r = torch.empty(w.M, dtype=torch.float32, device="cuda")
-        Z = g.coda_gemm_rowscale_rope(h, W2, cs, head_dim, rope_cols, P=P, eps=w.eps, r_out=r, positions=pos_d)
+        Z = g.coda_gemm_rowscale_rope(h, W2, head_dim, rope_cols, base, P=P, eps=w.eps, r_out=r, **kw)
     else:
         r = g.coda_rms_reduce(P, w.N, w.eps)
-        Z = g.coda_gemm_rowscale_rope(h, W2, cs, head_dim, rope_cols, r=r, positions=pos_d)
+        Z = g.coda_gemm_rowscale_rope(h, W2, head_dim, rope_cols, base, r=r, **kw)
     torch.cuda.synchronize()
     pos = np.arange(w.M) % n_pos if positions is None else np.asarray(positions)
     sel = slice(None) if rows is None else rows
