@@ -74,6 +74,8 @@ def _load():
             lib.coda_oracle_amax.restype = ctypes.c_double
             lib.coda_oracle_e4m3_fake_quant.argtypes = [_dp, _i64, _dp]
             lib.coda_oracle_e4m3_fake_quant.restype = ctypes.c_double
+            lib.coda_oracle_rmsnorm_backward.argtypes = [_dp, _dp, ctypes.c_double, _dp, _i64, _i64, _dp, _dp]
+            lib.coda_oracle_silu_mul_backward.argtypes = [_dp, _dp, _dp, _i64, _dp, _dp]
             lib.coda_oracle_rope.argtypes = [_dp, _i64, _i64, _i64, _i64, ctypes.POINTER(ctypes.c_int64),
                                              ctypes.c_double]
             _lib = lib
@@ -164,6 +166,24 @@ def rope(Z, rot_cols: int, head_dim: int, positions, base: float) -> np.ndarray:
     return Z
 
 
+def rmsnorm_backward(H, gamma, eps: float, dY):
+    """(dH, dgamma) of y = RMSNorm(h) * gamma for the upstream gradient dY."""
+    H, gamma, dY = _f64(H), _f64(gamma), _f64(dY)
+    M, N = H.shape
+    dH = np.empty_like(H)
+    dg = np.empty(N, dtype=np.float64)
+    _load().coda_oracle_rmsnorm_backward(_ptr(H), _ptr(gamma), float(eps), _ptr(dY), M, N, _ptr(dH), _ptr(dg))
+    return dH, dg
+
+
+def silu_mul_backward(G, U, dAct):
+    """(dG, dU) of act = silu(G) * U."""
+    G, U, dAct = _f64(G), _f64(U), _f64(dAct)
+    dG, dU = np.empty_like(G), np.empty_like(G)
+    _load().coda_oracle_silu_mul_backward(_ptr(G), _ptr(U), _ptr(dAct), G.size, _ptr(dG), _ptr(dU))
+    return dG, dU
+
+
 # --------------------------------------------------------------- blocks ----
 
 def block_rowscale(X, W1, R, gamma, W2, eps):
@@ -186,6 +206,37 @@ def block_rowscale_rope(X, W1, R, gamma, W2, eps, rot_cols, head_dim, positions,
     out = block_rowscale(X, W1, R, gamma, W2, eps)
     out["Z"] = rope(out["Z"], rot_cols, head_dim, positions, base)
     return out
+
+
+def block_rowscale_backward(X, W1, R, gamma, W2, eps, dZ, dH_in=None):
+    """Gradients of GEMM -> residual add -> RMSNorm -> GEMM (unfused) for the
+    upstream dZ and, optionally, dH_in flowing into h along the residual
+    stream.  Returns dX, dR (= dh), dW1 [K, N], dW2 [N, N2], dgamma."""
+    h = gemm(X, W1, R)
+    y, r = rmsnorm(h, gamma, eps)
+    dW2 = gemm(y.T.copy(), dZ)
+    dy = gemm(_f64(dZ), _f64(W2).T.copy())
+    dh, dgamma = rmsnorm_backward(h, gamma, eps, dy)
+    if dH_in is not None:
+        dh = dh + _f64(dH_in)
+    return {"dX": gemm(dh, _f64(W1).T.copy()), "dR": dh, "dW1": gemm(_f64(X).T.copy(), dh), "dW2": dW2,
+            "dgamma": dgamma, "h": h, "r": r}
+
+
+def block_swiglu_backward(X, W1, R, gamma, Wg, Wu, eps, dAct, dH_in=None):
+    """Gradients of GEMM -> residual add -> RMSNorm -> gate/up GEMMs -> SwiGLU
+    (unfused).  Returns dX, dR (= dh), dW1, dWg, dWu [N, I], dgamma."""
+    h = gemm(X, W1, R)
+    y, r = rmsnorm(h, gamma, eps)
+    G, U = gemm(y, Wg), gemm(y, Wu)
+    dG, dU = silu_mul_backward(G, U, dAct)
+    yT = y.T.copy()
+    dy = gemm(dG, _f64(Wg).T.copy()) + gemm(dU, _f64(Wu).T.copy())
+    dh, dgamma = rmsnorm_backward(h, gamma, eps, dy)
+    if dH_in is not None:
+        dh = dh + _f64(dH_in)
+    return {"dX": gemm(dh, _f64(W1).T.copy()), "dR": dh, "dW1": gemm(_f64(X).T.copy(), dh),
+            "dWg": gemm(yT, dG), "dWu": gemm(yT, dU), "dgamma": dgamma, "h": h, "r": r}
 
 
 def chain_full(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps):

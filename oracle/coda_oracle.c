@@ -165,3 +165,43 @@ void coda_oracle_rope(double *Z, int64_t M, int64_t N, int64_t rot_cols, int64_t
         }
     }
 }
+
+/* Backward of RMSNorm (LLaMA form y = h r gamma, r = 1/sqrt(mean h^2 + eps))
+ * for one upstream gradient dY [M x N]:
+ *   dH_ij    = r_i gamma_j dY_ij - h_ij r_i^3 / N * sum_k gamma_k dY_ik h_ik
+ *   dgamma_j = sum_i dY_ij h_ij r_i
+ * (differentiating y_ij = h_ij r_i gamma_j with d r_i / d h_ik = -r_i^3 h_ik / N).
+ * dgamma is written, not accumulated. */
+void coda_oracle_rmsnorm_backward(const double *H, const double *gamma, double eps, const double *dY,
+                                  int64_t M, int64_t N, double *dH, double *dgamma)
+{
+    for (int64_t j = 0; j < N; ++j)
+        dgamma[j] = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        const double *h = H + i * N, *dy = dY + i * N;
+        double ss = 0.0, dot = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            ss += h[j] * h[j];
+            dot += gamma[j] * dy[j] * h[j];
+        }
+        const double r = 1.0 / sqrt(ss / (double)N + eps);
+        for (int64_t j = 0; j < N; ++j) {
+            dH[i * N + j] = r * gamma[j] * dy[j] - h[j] * r * r * r / (double)N * dot;
+            dgamma[j] += dy[j] * h[j] * r;
+        }
+    }
+}
+
+/* Backward of SwiGLU gating act = silu(G) * U, silu(x) = x sigmoid(x):
+ *   dG = dAct * U * silu'(G),  silu'(x) = sigmoid(x) (1 + x (1 - sigmoid(x)))
+ *   dU = dAct * silu(G) */
+void coda_oracle_silu_mul_backward(const double *G, const double *U, const double *dAct, int64_t n,
+                                   double *dG, double *dU)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        const double s = 1.0 / (1.0 + exp(-G[i]));
+        dG[i] = dAct[i] * U[i] * s * (1.0 + G[i] * (1.0 - s));
+        dU[i] = dAct[i] * G[i] * s;
+    }
+}

@@ -265,3 +265,72 @@ def test_rope_scores_depend_only_on_relative_position():
     # and each pair keeps its length
     z = oracle.rope(q, d, d, np.array([777]), 500000.0)
     np.testing.assert_allclose(z[0, ::2] ** 2 + z[0, 1::2] ** 2, q[0, ::2] ** 2 + q[0, 1::2] ** 2, rtol=1e-12)
+
+
+# ------------------------------------------------------------- backward ----
+# The backward oracle is pinned by central finite differences of the forward
+# oracle: L = sum(dOut * out) + sum(dH_in * h), differentiated numerically in
+# every input element of tiny blocks.
+
+def _num_grad(f, arrays, name, eps=1e-6):
+    a = arrays[name]
+    g = np.zeros_like(a)
+    for idx in np.ndindex(a.shape):
+        old = a[idx]
+        a[idx] = old + eps
+        lp = f(arrays)
+        a[idx] = old - eps
+        lm = f(arrays)
+        a[idx] = old
+        g[idx] = (lp - lm) / (2 * eps)
+    return g
+
+
+@pytest.mark.parametrize("with_dh", [False, True])
+def test_rowscale_backward_matches_finite_differences(with_dh):
+    rng = np.random.default_rng(11)
+    M, K, N, N2 = 3, 4, 5, 6
+    A = {"X": rng.standard_normal((M, K)), "W1": rng.standard_normal((K, N)), "R": rng.standard_normal((M, N)),
+         "gamma": 1 + 0.1 * rng.standard_normal(N), "W2": rng.standard_normal((N, N2))}
+    dZ = rng.standard_normal((M, N2))
+    dH = rng.standard_normal((M, N)) if with_dh else None
+
+    def loss(a):
+        o = oracle.block_rowscale(a["X"], a["W1"], a["R"], a["gamma"], a["W2"], 1e-3)
+        return float(np.sum(dZ * o["Z"]) + (np.sum(dH * o["h"]) if with_dh else 0.0))
+    got = oracle.block_rowscale_backward(A["X"], A["W1"], A["R"], A["gamma"], A["W2"], 1e-3, dZ, dH)
+    for name, key in (("X", "dX"), ("W1", "dW1"), ("R", "dR"), ("gamma", "dgamma"), ("W2", "dW2")):
+        np.testing.assert_allclose(got[key], _num_grad(loss, A, name), rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+def test_swiglu_backward_matches_finite_differences():
+    rng = np.random.default_rng(12)
+    M, K, N, I = 3, 4, 5, 6
+    A = {"X": rng.standard_normal((M, K)), "W1": rng.standard_normal((K, N)), "R": rng.standard_normal((M, N)),
+         "gamma": 1 + 0.1 * rng.standard_normal(N), "Wg": rng.standard_normal((N, I)),
+         "Wu": rng.standard_normal((N, I))}
+    dAct = rng.standard_normal((M, I))
+    dH = rng.standard_normal((M, N))
+
+    def loss(a):
+        o = oracle.block_swiglu(a["X"], a["W1"], a["R"], a["gamma"], a["Wg"], a["Wu"], 1e-3)
+        return float(np.sum(dAct * o["act"]) + np.sum(dH * o["h"]))
+    got = oracle.block_swiglu_backward(A["X"], A["W1"], A["R"], A["gamma"], A["Wg"], A["Wu"], 1e-3, dAct, dH)
+    for name, key in (("X", "dX"), ("W1", "dW1"), ("R", "dR"), ("gamma", "dgamma"), ("Wg", "dWg"),
+                      ("Wu", "dWu")):
+        np.testing.assert_allclose(got[key], _num_grad(loss, A, name), rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+def test_silu_derivative_closed_form_and_norm_gradient_orthogonal_to_h():
+    # silu'(0) = 1/2, and silu' integrates back to silu (d/dG of silu(G) * 1)
+    dG, dU = oracle.silu_mul_backward(np.array([0.0, 2.0]), np.array([1.0, 1.0]), np.array([1.0, 1.0]))
+    assert dG[0] == pytest.approx(0.5, abs=1e-15)
+    s = 1 / (1 + math.exp(-2.0))
+    assert dG[1] == pytest.approx(s * (1 + 2 * (1 - s)), rel=1e-14)
+    assert dU[1] == pytest.approx(oracle.silu(2.0), rel=1e-14)
+    # with eps = 0 the normalised output ignores the row's scale, so the
+    # input gradient has no component along h
+    rng = np.random.default_rng(13)
+    H, dY = rng.standard_normal((4, 7)), rng.standard_normal((4, 7))
+    dH, _ = oracle.rmsnorm_backward(H, 1 + 0.1 * rng.standard_normal(7), 0.0, dY)
+    np.testing.assert_allclose(np.sum(dH * H, axis=1), 0.0, atol=1e-12)
