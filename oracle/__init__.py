@@ -251,6 +251,34 @@ def chain_full(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps):
     return {"h1": h1, "r1": r1, "act": act, "h2": h2, "r2": r2, "Z": gemm(y2, Wq)}
 
 
+def chain_full_backward(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps, dZ, dH2_in=None):
+    """Gradients of chain_full for the upstream dZ (of the QKV output) and,
+    optionally, dH2_in (of the residual stream h2).  Unfused fp64: the
+    forward is recomputed, then each step's derivative in reverse order."""
+    f = chain_full(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps)
+    h1, h2 = f["h1"], f["h2"]
+    y1, _ = rmsnorm(h1, gamma1, eps)
+    y2, _ = rmsnorm(h2, gamma2, eps)
+    G, U = gemm(y1, Wg), gemm(y1, Wu)
+    T = lambda a: _f64(a).T.copy()  # noqa: E731
+    # Z = y2 Wq
+    dWq = gemm(T(y2), dZ)
+    dh2, dgamma2 = rmsnorm_backward(h2, gamma2, eps, gemm(dZ, T(Wq)))
+    if dH2_in is not None:
+        dh2 = dh2 + _f64(dH2_in)
+    # h2 = h1 + act Wd
+    dAct = gemm(dh2, T(Wd))
+    dWd = gemm(T(f["act"]), dh2)
+    # act = silu(G) U, G = y1 Wg, U = y1 Wu
+    dG, dU = silu_mul_backward(G, U, dAct)
+    dWg, dWu = gemm(T(y1), dG), gemm(T(y1), dU)
+    dh1, dgamma1 = rmsnorm_backward(h1, gamma1, eps, gemm(dG, T(Wg)) + gemm(dU, T(Wu)))
+    dh1 = dh1 + dh2
+    # h1 = R + X Wo
+    return {"dX": gemm(dh1, T(Wo)), "dR": dh1, "dWo": gemm(T(X), dh1), "dWg": dWg, "dWu": dWu, "dWd": dWd,
+            "dWq": dWq, "dgamma1": dgamma1, "dgamma2": dgamma2, "dh2": dh2, "dG": dG, "dU": dU}
+
+
 def chain_full_fp8(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps, out_rows=None):
     """Quantisation-aware FP8 chain.  FP8 changes the arithmetic, so here the
     oracle follows the reparameterised steps and quantises exactly the GEMM

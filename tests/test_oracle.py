@@ -334,3 +334,21 @@ def test_silu_derivative_closed_form_and_norm_gradient_orthogonal_to_h():
     H, dY = rng.standard_normal((4, 7)), rng.standard_normal((4, 7))
     dH, _ = oracle.rmsnorm_backward(H, 1 + 0.1 * rng.standard_normal(7), 0.0, dY)
     np.testing.assert_allclose(np.sum(dH * H, axis=1), 0.0, atol=1e-12)
+
+
+def test_chain_backward_matches_finite_differences():
+    rng = np.random.default_rng(14)
+    M, K, H, I, Q = 2, 3, 4, 5, 3
+    A = {"X": rng.standard_normal((M, K)), "Wo": rng.standard_normal((K, H)), "R": rng.standard_normal((M, H)),
+         "g1": 1 + 0.1 * rng.standard_normal(H), "Wg": rng.standard_normal((H, I)), "Wu": rng.standard_normal((H, I)),
+         "Wd": rng.standard_normal((I, H)), "g2": 1 + 0.1 * rng.standard_normal(H), "Wq": rng.standard_normal((H, Q))}
+    dZ, dH2 = rng.standard_normal((M, Q)), rng.standard_normal((M, H))
+
+    def loss(a):
+        o = oracle.chain_full(a["X"], a["Wo"], a["R"], a["g1"], a["Wg"], a["Wu"], a["Wd"], a["g2"], a["Wq"], 1e-3)
+        return float(np.sum(dZ * o["Z"]) + np.sum(dH2 * o["h2"]))
+    got = oracle.chain_full_backward(A["X"], A["Wo"], A["R"], A["g1"], A["Wg"], A["Wu"], A["Wd"], A["g2"], A["Wq"],
+                                     1e-3, dZ, dH2)
+    for name, key in (("X", "dX"), ("R", "dR"), ("Wo", "dWo"), ("g1", "dgamma1"), ("Wg", "dWg"), ("Wu", "dWu"),
+                      ("Wd", "dWd"), ("g2", "dgamma2"), ("Wq", "dWq")):
+        np.testing.assert_allclose(got[key], _num_grad(loss, A, name), rtol=1e-6, atol=1e-8, err_msg=name)
