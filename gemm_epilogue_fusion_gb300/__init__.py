@@ -32,6 +32,7 @@ from . import _build
 
 CODA_OK, CODA_ERR_INVALID_ARG, CODA_ERR_UNSUPPORTED, CODA_ERR_CUDA, CODA_ERR_TIMEOUT = range(5)
 CODA_F32, CODA_BF16, CODA_E4M3 = 0, 1, 2
+CODA_K_MAJOR, CODA_MN_MAJOR = 0, 1
 
 _STATUS_NAMES = {0: "CODA_OK", 1: "CODA_ERR_INVALID_ARG", 2: "CODA_ERR_UNSUPPORTED", 3: "CODA_ERR_CUDA",
                  4: "CODA_ERR_TIMEOUT"}
@@ -60,6 +61,12 @@ SIGNATURES = {
                                          _i32, _vp]),
     "coda_gemm_rowscale_rope": (_i32, [_vp, _vp, _fp, _fp, _f32, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _i64,
                                        _i64, ctypes.c_double, _i64, _vp, _vp]),
+    "coda_gemm": (_i32, [_vp, _i32, _vp, _i32, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _vp]),
+    "coda_gemm_grad_norm": (_i32, [_vp, _vp, _vp, _fp, _vp, _fp, _i64, _i64, _i64, _i32, _vp]),
+    "coda_rmsnorm_backward_workspace_bytes": (_i64, [_i64, _i64]),
+    "coda_rmsnorm_backward": (_i32, [_vp, _vp, _fp, _fp, _fp, _vp, _vp, _vp, _fp, _fp, _i64, _i64, _vp]),
+    "coda_gemm_swiglu_backward": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
+    "coda_gemm_swiglu_save": (_i32, [_vp, _vp, _vp, _fp, _fp, _f32, _fp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
     "coda_amax": (_i32, [_vp, _i64, _i32, _fp, _vp]),
     "coda_quantize_e4m3": (_i32, [_vp, _i64, _i32, _fp, _vp, _fp, _vp]),
     "coda_get_device_status": (_i32, []),
@@ -250,6 +257,83 @@ def coda_gemm_rowscale_rope(H, W2t, head_dim: int, rope_cols: int, base: float, 
                                        _dev(scale_w, "scale_w"), head_dim, rope_cols, float(base), seq_len,
                                        _dev(positions, "positions"), _stream(H, stream)))
     return Z
+
+
+def coda_gemm(A, B, *, a_mn: bool = False, b_mn: bool = False, row_scale=None, col_scale=None, D=None,
+              stream=None):
+    """D = diag(row_scale) opA(A) opB(B)^T diag(col_scale), with opA(A) = A [M, K] or A^T for A [K, M]
+    (a_mn) and opB(B) = B [N, K] or B^T for B [K, N] (b_mn)."""
+    lib = load_library()
+    M, K = (A.shape[1], A.shape[0]) if a_mn else (A.shape[0], A.shape[1])
+    N = B.shape[1] if b_mn else B.shape[0]
+    if (B.shape[0] if b_mn else B.shape[1]) != K:
+        raise ValueError("inner dimensions differ")
+    code = _dtype_code(A)
+    if D is None:
+        D = torch.empty(M, N, dtype=_out_dtype(code), device=A.device)
+    _check(lib.coda_gemm(_dev(A, "A"), int(a_mn), _dev(B, "B"), int(b_mn), _dev(D, "D"), M, N, K, code,
+                         _dev(row_scale, "row_scale"), _dev(col_scale, "col_scale"), _stream(A, stream)))
+    return D
+
+
+def coda_gemm_grad_norm(dOut, Wt, H, gamma, dY=None, S=None, stream=None):
+    """dY = dOut . Wt (Wt [K, N] as the forward stores it) and S = per-group sums of gamma dY H.  Returns (dY, S)."""
+    lib = load_library()
+    M, K = dOut.shape
+    N = Wt.shape[1]
+    if dY is None:
+        dY = torch.empty(M, N, dtype=torch.bfloat16, device=dOut.device)
+    if S is None:
+        S = torch.empty(M, coda_partial_cols(N), dtype=torch.float32, device=dOut.device)
+    _check(lib.coda_gemm_grad_norm(_dev(dOut, "dOut"), _dev(Wt, "Wt"), _dev(H, "H"), _dev(gamma, "gamma"),
+                                   _dev(dY, "dY"), _dev(S, "S"), M, N, K, _dtype_code(dOut), _stream(dOut, stream)))
+    return dY, S
+
+
+def coda_rmsnorm_backward(dY, H, r, gamma, S, dH_in=None, dH=None, Yt=None, dgamma=None, workspace=None,
+                          stream=None):
+    """dH = r gamma dY - c H (+ dH_in), Yt = r H, dgamma.  Returns (dH, Yt, dgamma)."""
+    lib = load_library()
+    M, N = dY.shape
+    dH = torch.empty_like(dY) if dH is None else dH
+    Yt = torch.empty_like(dY) if Yt is None else Yt
+    if dgamma is None:
+        dgamma = torch.empty(N, dtype=torch.float32, device=dY.device)
+    if workspace is None:
+        n = lib.coda_rmsnorm_backward_workspace_bytes(M, N)
+        workspace = torch.empty(max(n // 4, 1), dtype=torch.float32, device=dY.device)
+    _check(lib.coda_rmsnorm_backward(_dev(dY, "dY"), _dev(H, "H"), _dev(r, "r"), _dev(gamma, "gamma"), _dev(S, "S"),
+                                     _dev(dH_in, "dH_in"), _dev(dH, "dH"), _dev(Yt, "Yt"), _dev(dgamma, "dgamma"),
+                                     _dev(workspace, "workspace"), M, N, _stream(dY, stream)))
+    return dH, Yt, dgamma
+
+
+def coda_gemm_swiglu_save(H, Wgt, Wut, *, r=None, P=None, eps: float = 0.0, r_out=None, Act=None, GU=None,
+                          stream=None):
+    """SwiGLU GEMM that also returns the pre-activations G || U [M, 2I].  Returns (Act, GU)."""
+    lib = load_library()
+    M, K = H.shape
+    I = Wgt.shape[0]
+    if Act is None:
+        Act = torch.empty(M, I, dtype=torch.bfloat16, device=H.device)
+    if GU is None:
+        GU = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=H.device)
+    _check(lib.coda_gemm_swiglu_save(_dev(H, "H"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"), _dev(r, "r"), _dev(P, "P"),
+                                     float(eps), _dev(r_out, "r_out"), _dev(Act, "Act"), _dev(GU, "GU"), M, I, K,
+                                     _dtype_code(H), _stream(H, stream)))
+    return Act, GU
+
+
+def coda_gemm_swiglu_backward(dOut, Wt, GU, dGU=None, stream=None):
+    """dG || dU from dAct = dOut . Wt (Wt [K, I]) and the saved G || U [M, 2I]."""
+    lib = load_library()
+    M, K = dOut.shape
+    I = Wt.shape[1]
+    if dGU is None:
+        dGU = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dOut.device)
+    _check(lib.coda_gemm_swiglu_backward(_dev(dOut, "dOut"), _dev(Wt, "Wt"), _dev(GU, "GU"), _dev(dGU, "dGU"), M, I,
+                                         K, _dtype_code(dOut), _stream(dOut, stream)))
+    return dGU
 
 
 def coda_block_workspace_bytes(M: int) -> int:

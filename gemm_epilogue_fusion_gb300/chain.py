@@ -131,3 +131,50 @@ def full_chain_fp8(X, R, Wq8: Dict[str, tuple], eps: float, bufs: Optional[dict]
     b.update({"Xq": Xq, "sx": sx, "h1": h1, "P1": P1, "r1": r1, "h1q": h1q, "s1": s1, "act": act, "actq": actq,
               "s2": s2, "h2": h2, "P2": P2, "r2": r2, "h2q": h2q, "s3": s3, "Z": Z})
     return b
+
+
+# ------------------------------------------------------------- backward ----
+# Gradients of the blocks above (bf16), each step one of the library's calls:
+#   coda_gemm_grad_norm      dy = dOut . W with the RMSNorm backward's row sums
+#   coda_rmsnorm_backward    dh, r h, dgamma
+#   coda_gemm (MN-major)     dX = dh . W1, dW = X^T dh, dW2 = (r h)^T dZ diag(gamma)
+#   coda_gemm_swiglu_backward  dG, dU in the epilogue of dAct = dh2 . Wd
+# Weights are the unfolded W^T [N_out, K] the forward folded gamma into.
+
+def rowscale_block_backward(X, W1t, W2t, gamma, h, r, dZ, dH_in=None) -> dict:
+    """Gradients of rowscale_block: dX, dR (= dh), dW1t, dW2t, dgamma."""
+    from . import coda_gemm, coda_gemm_grad_norm, coda_rmsnorm_backward
+    dy, S = coda_gemm_grad_norm(dZ, W2t, h, gamma)
+    dh, Yt, dgamma = coda_rmsnorm_backward(dy, h, r, gamma, S, dH_in)
+    return {"dX": coda_gemm(dh, W1t, b_mn=True), "dR": dh, "dW1t": coda_gemm(dh, X, a_mn=True, b_mn=True),
+            "dW2t": coda_gemm(dZ, Yt, a_mn=True, b_mn=True, col_scale=gamma), "dgamma": dgamma}
+
+
+def full_chain_train_forward(X, Wot, R, Wgt_f, Wut_f, Wdt, Wqt_f, eps: float) -> dict:
+    """full_chain with the reductions in the consumers' epilogues, saving what
+    the backward needs: r1, r2 and the SwiGLU pre-activations G || U."""
+    from . import coda_gemm_swiglu_save
+    h1, P1 = coda_gemm_residual_partial_rms(X, Wot, R)
+    r1 = torch.empty(X.shape[0], dtype=torch.float32, device=X.device)
+    act, GU = coda_gemm_swiglu_save(h1, Wgt_f, Wut_f, P=P1, eps=eps, r_out=r1)
+    h2, P2 = coda_gemm_residual_partial_rms(act, Wdt, h1)
+    r2 = torch.empty_like(r1)
+    Z = coda_gemm_rowscale_fused_rms(h2, Wqt_f, P2, eps, None, r2)
+    return {"h1": h1, "r1": r1, "act": act, "GU": GU, "h2": h2, "r2": r2, "Z": Z}
+
+
+def full_chain_backward(X, Wot, Wgut, Wdt, Wqt, gamma1, gamma2, fwd: dict, dZ, dH2_in=None) -> dict:
+    """Gradients of full_chain from the saved forward state.  Wgut is the
+    unfolded gate and up weights stacked [2I, H] (Wgt above Wut)."""
+    from . import coda_gemm, coda_gemm_grad_norm, coda_gemm_swiglu_backward, coda_rmsnorm_backward
+    dy2, S2 = coda_gemm_grad_norm(dZ, Wqt, fwd["h2"], gamma2)
+    dh2, Yt2, dgamma2 = coda_rmsnorm_backward(dy2, fwd["h2"], fwd["r2"], gamma2, S2, dH2_in)
+    dWqt = coda_gemm(dZ, Yt2, a_mn=True, b_mn=True, col_scale=gamma2)
+    dGU = coda_gemm_swiglu_backward(dh2, Wdt, fwd["GU"])
+    dWdt = coda_gemm(dh2, fwd["act"], a_mn=True, b_mn=True)
+    dy1, S1 = coda_gemm_grad_norm(dGU, Wgut, fwd["h1"], gamma1)
+    dh1, Yt1, dgamma1 = coda_rmsnorm_backward(dy1, fwd["h1"], fwd["r1"], gamma1, S1, dh2)
+    dWgut = coda_gemm(dGU, Yt1, a_mn=True, b_mn=True, col_scale=gamma1)
+    return {"dX": coda_gemm(dh1, Wot, b_mn=True), "dR": dh1, "dWot": coda_gemm(dh1, X, a_mn=True, b_mn=True),
+            "dWgut": dWgut, "dWdt": dWdt, "dWqt": dWqt, "dgamma1": dgamma1, "dgamma2": dgamma2, "dh2": dh2,
+            "dGU": dGU}

@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <utility>
 
 #include "coda.h"
 #include "coda_internal.h"
@@ -500,6 +501,197 @@ coda_status coda_gemm_swiglu_fused_rms(const void* H, const void* Wgt, const voi
   }
   return gemm_swiglu_impl(H, Wgt, Wut, nullptr, P, eps, r_out, Act, M, I, K, dtype, scale_h, scale_wg, scale_wu,
                           amax_act, stream);
+}
+
+coda_status coda_gemm(const void* A, coda_layout a_layout, const void* B, coda_layout b_layout, void* D, int64_t M,
+                      int64_t N, int64_t K, coda_dtype dtype, const float* row_scale, const float* col_scale,
+                      cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(dtype == CODA_F32 || dtype == CODA_BF16, "coda_gemm: dtype must be CODA_F32 or CODA_BF16");
+  REQUIRE((a_layout == CODA_K_MAJOR || a_layout == CODA_MN_MAJOR) && (b_layout == CODA_K_MAJOR || b_layout == CODA_MN_MAJOR),
+          "unknown layout");
+  const bool a_mn = a_layout == CODA_MN_MAJOR, b_mn = b_layout == CODA_MN_MAJOR;
+  REQUIRE(!(a_mn || b_mn) || dtype == CODA_BF16, "MN-major operands are bf16 only");
+  REQUIRE(!(a_mn && !b_mn), "an MN-major A needs an MN-major B");
+  REQUIRE(M >= 0 && M < INT32_MAX && N > 0 && N < INT32_MAX && K > 0 && K < INT32_MAX, "bad shape");
+  const int eb = elem_bytes(dtype), ob = out_bytes(dtype);
+  REQUIRE(((a_mn ? M : K) * eb) % 16 == 0, "A's rows must be a multiple of 16 bytes");
+  REQUIRE(((b_mn ? N : K) * eb) % 16 == 0, "B's rows must be a multiple of 16 bytes");
+  REQUIRE((N * ob) % 16 == 0, "D's rows must be a multiple of 16 bytes");
+  if (M == 0) return CODA_OK;
+  TRY(check_ptr(A, "A"));
+  TRY(check_ptr(B, "B"));
+  TRY(check_ptr(D, "D"));
+  if (row_scale) TRY(check_scalar_ptr(row_scale, "row_scale"));
+  if (col_scale) TRY(check_scalar_ptr(col_scale, "col_scale"));
+  const Range outs[] = {rng("D", D, M * N * ob)};
+  const Range ins[] = {rng("A", A, M * K * eb), rng("B", B, N * K * eb),
+                       rng("row_scale", row_scale, row_scale ? M * 4 : 0),
+                       rng("col_scale", col_scale, col_scale ? N * 4 : 0)};
+  TRY(check_overlaps(outs, 1, ins, 4));
+  coda::GemmProblem p = {};
+  p.epi = coda::kEpiRowScale;
+  p.A = A;
+  p.B = B;
+  p.D = D;
+  p.M = static_cast<int>(M);
+  p.N_out = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.ep.r = row_scale;
+  p.ep.col_scale = col_scale;
+  p.a_mn = a_mn;
+  p.b_mn = b_mn;
+  p.stream = stream;
+  p.pdl = use_pdl();
+  return run_gemm(dtype, p);
+}
+
+coda_status coda_gemm_grad_norm(const void* dOut, const void* Wt, const void* H, const float* gamma, void* dY,
+                                float* S, int64_t M, int64_t N, int64_t K, coda_dtype dtype, cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(dtype == CODA_BF16, "coda_gemm_grad_norm: dtype must be CODA_BF16");
+  TRY(check_gemm_dims(M, N, K, dtype, "N"));
+  if (M == 0) return CODA_OK;
+  TRY(check_ptr(dOut, "dOut"));
+  TRY(check_ptr(Wt, "Wt"));
+  TRY(check_ptr(H, "H"));
+  TRY(check_ptr(gamma, "gamma"));
+  TRY(check_ptr(dY, "dY"));
+  TRY(check_ptr(S, "S"));
+  const int64_t T = coda_partial_cols(N);
+  const Range outs[] = {rng("dY", dY, M * N * 2), rng("S", S, M * T * 4)};
+  const Range ins[] = {rng("dOut", dOut, M * K * 2), rng("Wt", Wt, K * N * 2), rng("H", H, M * N * 2),
+                       rng("gamma", gamma, N * 4)};
+  TRY(check_overlaps(outs, 2, ins, 4));
+  coda::GemmProblem p = {};
+  p.epi = coda::kEpiGradNorm;
+  p.A = dOut;
+  p.B = Wt;
+  p.R = H;
+  p.D = dY;
+  p.M = static_cast<int>(M);
+  p.N_out = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.ep.P = S;
+  p.ep.T = static_cast<int>(T);
+  p.ep.col_scale = gamma;
+  p.b_mn = true;
+  p.stream = stream;
+  p.pdl = use_pdl();
+  return run_gemm(dtype, p);
+}
+
+int64_t coda_rmsnorm_backward_workspace_bytes(int64_t M, int64_t N) {
+  if (M < 0 || N <= 0) return -1;
+  return coda::rmsnorm_bwd_chunks(M) * N * static_cast<int64_t>(sizeof(float));
+}
+
+coda_status coda_rmsnorm_backward(const void* dY, const void* H, const float* r, const float* gamma, const float* S,
+                                  const void* dH_in, void* dH, void* Yt, float* dgamma, float* workspace, int64_t M,
+                                  int64_t N, cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(M >= 0 && M < INT32_MAX && N > 0 && N < INT32_MAX && N % 8 == 0,
+          "coda_rmsnorm_backward: M in [0, 2^31), N a positive multiple of 8");
+  if (M == 0) {
+    TRY(check_scalar_ptr(dgamma, "dgamma"));
+    cudaError_t e = cudaMemsetAsync(dgamma, 0, static_cast<size_t>(N) * sizeof(float), stream);
+    return e == cudaSuccess ? CODA_OK : cuda_fail(e, "cudaMemsetAsync(dgamma)");
+  }
+  for (const auto& pr : {std::make_pair(dY, "dY"), std::make_pair(H, "H"), std::make_pair(static_cast<const void*>(dH), "dH"),
+                         std::make_pair(static_cast<const void*>(Yt), "Yt"), std::make_pair(static_cast<const void*>(gamma), "gamma"),
+                         std::make_pair(static_cast<const void*>(dgamma), "dgamma"),
+                         std::make_pair(static_cast<const void*>(workspace), "workspace")})
+    TRY(check_ptr(pr.first, pr.second));
+  TRY(check_scalar_ptr(r, "r"));
+  TRY(check_scalar_ptr(S, "S"));
+  if (dH_in) TRY(check_ptr(dH_in, "dH_in"));
+  const int64_t T = coda_partial_cols(N);
+  const int64_t mn = M * N * 2;
+  const Range outs[] = {rng("dH", dH, mn), rng("Yt", Yt, mn), rng("dgamma", dgamma, N * 4),
+                        rng("workspace", workspace, coda_rmsnorm_backward_workspace_bytes(M, N))};
+  const Range ins[] = {rng("dY", dY, mn), rng("H", H, mn), rng("r", r, M * 4), rng("gamma", gamma, N * 4),
+                       rng("S", S, M * T * 4), rng("dH_in", dH_in, dH_in ? mn : 0)};
+  TRY(check_overlaps(outs, 4, ins, 6));
+  cudaError_t e = coda::launch_rmsnorm_backward(dY, H, r, gamma, S, static_cast<int>(T), dH_in, dH, Yt, dgamma,
+                                                workspace, M, N, stream);
+  return e == cudaSuccess ? CODA_OK : cuda_fail(e, "coda_rmsnorm_backward launch");
+}
+
+coda_status coda_gemm_swiglu_save(const void* H, const void* Wgt, const void* Wut, const float* r, const float* P,
+                                  float eps, float* r_out, void* Act, void* GU, int64_t M, int64_t I, int64_t K,
+                                  coda_dtype dtype, cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(dtype == CODA_BF16, "coda_gemm_swiglu_save: dtype must be CODA_BF16");
+  // a 64-column box of the G half must not reach into the U half
+  REQUIRE(I % 64 == 0, "coda_gemm_swiglu_save: I must be a multiple of 64");
+  REQUIRE(M <= 0 || (r == nullptr) != (P == nullptr), "exactly one of r and P must be given");
+  TRY(check_gemm_dims(M, I, K, dtype, "I"));
+  if (P) REQUIRE(std::isfinite(eps) && eps >= 0.0f, "eps must be finite and >= 0");
+  if (M == 0) return CODA_OK;
+  TRY(check_ptr(H, "H"));
+  TRY(check_ptr(Wgt, "Wgt"));
+  TRY(check_ptr(Wut, "Wut"));
+  TRY(check_ptr(Act, "Act"));
+  TRY(check_ptr(GU, "GU"));
+  if (P) TRY(check_ptr(P, "P"));
+  else TRY(check_scalar_ptr(r, "r"));
+  if (r_out) TRY(check_scalar_ptr(r_out, "r_out"));
+  const int64_t T = coda_partial_cols(K);
+  const Range outs[] = {rng("Act", Act, M * I * 2), rng("GU", GU, M * 2 * I * 2),
+                        rng("r_out", r_out, (P && r_out) ? M * 4 : 0)};
+  const Range ins[] = {rng("H", H, M * K * 2), rng("Wgt", Wgt, I * K * 2), rng("Wut", Wut, I * K * 2),
+                       rng("r", r, r ? M * 4 : 0), rng("P", P, P ? M * T * 4 : 0)};
+  TRY(check_overlaps(outs, 3, ins, 5));
+  coda::GemmProblem p = {};
+  p.epi = coda::kEpiSwiGLUSave;
+  p.A = H;
+  p.B = Wgt;
+  p.B2 = Wut;
+  p.D = Act;
+  p.GU = GU;
+  p.M = static_cast<int>(M);
+  p.N_out = static_cast<int>(I);
+  p.K = static_cast<int>(K);
+  p.ep.r = P ? nullptr : r;
+  p.ep.P_in = P;
+  p.ep.T_in = static_cast<int>(T);
+  p.ep.n_norm = static_cast<float>(K);
+  p.ep.eps = eps;
+  p.ep.r_out = P ? r_out : nullptr;
+  p.ep.gu_off = static_cast<int>(I);
+  p.stream = stream;
+  p.pdl = use_pdl();
+  return run_gemm(dtype, p);
+}
+
+coda_status coda_gemm_swiglu_backward(const void* dOut, const void* Wt, const void* GU, void* dGU, int64_t M,
+                                      int64_t I, int64_t K, coda_dtype dtype, cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(dtype == CODA_BF16, "coda_gemm_swiglu_backward: dtype must be CODA_BF16");
+  REQUIRE(I % 64 == 0, "coda_gemm_swiglu_backward: I must be a multiple of 64");
+  TRY(check_gemm_dims(M, I, K, dtype, "I"));
+  if (M == 0) return CODA_OK;
+  TRY(check_ptr(dOut, "dOut"));
+  TRY(check_ptr(Wt, "Wt"));
+  TRY(check_ptr(GU, "GU"));
+  TRY(check_ptr(dGU, "dGU"));
+  const Range outs[] = {rng("dGU", dGU, M * 2 * I * 2)};
+  const Range ins[] = {rng("dOut", dOut, M * K * 2), rng("Wt", Wt, K * I * 2), rng("GU", GU, M * 2 * I * 2)};
+  TRY(check_overlaps(outs, 1, ins, 3));
+  coda::GemmProblem p = {};
+  p.epi = coda::kEpiSwiGLUBwd;
+  p.A = dOut;
+  p.B = Wt;
+  p.R = GU;
+  p.D = dGU;
+  p.M = static_cast<int>(M);
+  p.N_out = static_cast<int>(I);
+  p.K = static_cast<int>(K);
+  p.ep.gu_off = static_cast<int>(I);
+  p.b_mn = true;
+  p.stream = stream;
+  p.pdl = use_pdl();
+  return run_gemm(dtype, p);
 }
 
 int64_t coda_block_workspace_bytes(int64_t M) {

@@ -169,6 +169,81 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   }
 }
 
+// RMSNorm backward on [M, N] (y = h r gamma), given dY and the grad-norm
+// GEMM's partials S[i, g] = sum over group g of gamma_j dY_ij h_ij:
+//   c_i   = r_i^3 / N * sum_g S[i, g]
+//   dh_ij = r_i gamma_j dY_ij - c_i h_ij (+ dH_in_ij)
+//   Yt_ij = r_i h_ij                       (the weight gradient's operand)
+//   part[chunk, j] = sum over the chunk's rows of dY_ij h_ij r_i  (dgamma partials)
+// Block: kBwdThreads threads x 8 columns each, one chunk of kBwdRows rows.
+constexpr int kBwdRows = 64;
+constexpr int kBwdThreads = 128;
+
+__global__ void __launch_bounds__(kBwdThreads) rmsnorm_bwd_kernel(
+    const uint4* __restrict__ dY, const uint4* __restrict__ H, const float* __restrict__ r,
+    const float* __restrict__ gamma, const float* __restrict__ S, int T, const uint4* __restrict__ dH_in,
+    uint4* __restrict__ dH, uint4* __restrict__ Yt, float* __restrict__ part, int M, int N) {
+  __shared__ float s_r[kBwdRows], s_c[kBwdRows];
+  const int row0 = blockIdx.y * kBwdRows;
+  if (threadIdx.x < kBwdRows) {
+    const int i = row0 + threadIdx.x;
+    float ri = 0.0f, ci = 0.0f;
+    if (i < M) {
+      ri = r[i];
+      float sum = 0.0f;
+      for (int t = 0; t < T; ++t) sum += S[static_cast<int64_t>(i) * T + t];
+      ci = ri * ri * ri / static_cast<float>(N) * sum;
+    }
+    s_r[threadIdx.x] = ri;
+    s_c[threadIdx.x] = ci;
+  }
+  __syncthreads();
+  const int col = (blockIdx.x * kBwdThreads + threadIdx.x) * 8;
+  if (col >= N) return;
+  float g[8], dg[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    g[e] = __ldg(gamma + col + e);
+    dg[e] = 0.0f;
+  }
+  const int nv = N / 8;
+  const int rows = min(kBwdRows, M - row0);
+  for (int ii = 0; ii < rows; ++ii) {
+    const int64_t v = static_cast<int64_t>(row0 + ii) * nv + col / 8;
+    const float ri = s_r[ii], ci = s_c[ii];
+    uint4 a = __ldg(dY + v), b = __ldg(H + v), d = dH_in ? __ldg(dH_in + v) : make_uint4(0, 0, 0, 0);
+    const __nv_bfloat162* ya = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&b);
+    const __nv_bfloat162* dd = reinterpret_cast<const __nv_bfloat162*>(&d);
+    uint4 o1, o2;
+    __nv_bfloat162* w1 = reinterpret_cast<__nv_bfloat162*>(&o1);
+    __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(&o2);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 y = __bfloat1622float2(ya[e]), h = __bfloat1622float2(hb[e]), x = __bfloat1622float2(dd[e]);
+      w1[e] = __floats2bfloat162_rn(ri * g[2 * e] * y.x - ci * h.x + x.x, ri * g[2 * e + 1] * y.y - ci * h.y + x.y);
+      w2[e] = __floats2bfloat162_rn(ri * h.x, ri * h.y);
+      dg[2 * e] += y.x * h.x * ri;
+      dg[2 * e + 1] += y.y * h.y * ri;
+    }
+    dH[v] = o1;
+    Yt[v] = o2;
+  }
+  float4* pp = reinterpret_cast<float4*>(part + static_cast<int64_t>(blockIdx.y) * N + col);
+  pp[0] = make_float4(dg[0], dg[1], dg[2], dg[3]);
+  pp[1] = make_float4(dg[4], dg[5], dg[6], dg[7]);
+}
+
+// dgamma[j] = sum over chunks of part[chunk, j], in chunk order.
+__global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict__ part, int chunks, int N,
+                                                         float* __restrict__ out) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= N) return;
+  float s = 0.0f;
+  for (int c = 0; c < chunks; ++c) s += part[static_cast<int64_t>(c) * N + j];
+  out[j] = s;
+}
+
 int grid_for(int64_t work_items, int threads) {
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
   int64_t g = (work_items + threads - 1) / threads;
@@ -197,6 +272,22 @@ cudaError_t launch_fold_gamma(const void* Wt, const float* gamma, void* Wt_out, 
   else
     fold_gamma_kernel<false><<<g, 256, 0, s>>>(static_cast<const uint4*>(Wt), gamma, static_cast<uint4*>(Wt_out),
                                                n_vec, K);
+  return cudaGetLastError();
+}
+
+int64_t rmsnorm_bwd_chunks(int64_t M) { return (M + kBwdRows - 1) / kBwdRows; }
+
+cudaError_t launch_rmsnorm_backward(const void* dY, const void* H, const float* r, const float* gamma,
+                                    const float* S, int T, const void* dH_in, void* dH, void* Yt, float* dgamma,
+                                    float* part, int64_t M, int64_t N, cudaStream_t s) {
+  const int chunks = static_cast<int>(rmsnorm_bwd_chunks(M));
+  const dim3 grid(static_cast<unsigned>((N / 8 + kBwdThreads - 1) / kBwdThreads), static_cast<unsigned>(chunks));
+  rmsnorm_bwd_kernel<<<grid, kBwdThreads, 0, s>>>(
+      static_cast<const uint4*>(dY), static_cast<const uint4*>(H), r, gamma, S, T, static_cast<const uint4*>(dH_in),
+      static_cast<uint4*>(dH), static_cast<uint4*>(Yt), part, static_cast<int>(M), static_cast<int>(N));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  column_sum_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(part, chunks, static_cast<int>(N), dgamma);
   return cudaGetLastError();
 }
 

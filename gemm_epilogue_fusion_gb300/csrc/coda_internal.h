@@ -25,7 +25,22 @@ __device__ __forceinline__ float row_rstd(const float* __restrict__ p, int T, fl
 }
 
 // Epilogue programs of the persistent GEMM (see gemm_epilogue.cuh).
-enum Epilogue { kEpiResidualPartialRms = 0, kEpiRowScale = 1, kEpiSwiGLU = 2 };
+// Backward programs:
+//   kEpiGradNorm   dY = acc stored; P[row, g] = sum over the 128-column group g of
+//                  col_scale_j * dY_j * H_j, with H TMA-loaded (RMSNorm backward's
+//                  row reduction, on the stored dY)
+//   kEpiSwiGLUBwd  acc = dAct; with the saved pre-activations G, U loaded:
+//                  dG = dAct U silu'(G), dU = dAct silu(G), stored side by side
+//   kEpiSwiGLUSave SwiGLU that also stores the pre-activations G = r g and
+//                  U = r u (bf16) side by side, for the backward
+enum Epilogue {
+  kEpiResidualPartialRms = 0,
+  kEpiRowScale = 1,
+  kEpiSwiGLU = 2,
+  kEpiGradNorm = 3,
+  kEpiSwiGLUBwd = 4,
+  kEpiSwiGLUSave = 5
+};
 
 // Width, in output columns, of one partial sum-of-squares group written by the
 // residual epilogue: P has ceil(N / kPartialCols) columns.
@@ -51,6 +66,9 @@ struct EpiParams {
   const int* rope_pos;    // [M] positions; null = row % rope_seq
   int rope_seq, rope_half, rope_cols;
   float rope_log2b;       // log2(base) / rope_half
+  const float* col_scale; // row-scale program: nullable [N_out], multiplies output column n;
+                          // grad-norm program: gamma [N_out]
+  int gu_off;             // SwiGLU backward: column offset of U (and dU) in the [M, 2 I] tensors
 };
 
 // Second phase of a two-phase launch (the consuming GEMM of the block).
@@ -75,6 +93,9 @@ struct GemmProblem {
   EpiParams ep;
   cudaStream_t stream;
   bool pdl;                // launch with programmatic stream serialisation
+  void* GU = nullptr;      // kEpiSwiGLUSave: G || U output [M, 2 N_out]
+  bool a_mn = false;       // A stored [K, M] (MN-major) instead of [M, K]
+  bool b_mn = false;       // B stored [K, N_out] instead of [N_out, K]
   PhaseB b;                // consuming GEMM of a two-phase launch
   unsigned* band_ready;    // two-phase: [ceil(M / tile rows) + 1] zeroed counters
 };
@@ -94,6 +115,10 @@ cudaError_t launch_rms_reduce(const float* P, int64_t M, int T, int64_t N, float
                               cudaStream_t s, bool pdl);
 cudaError_t launch_fold_gamma(const void* Wt, const float* gamma, void* Wt_out, int64_t N_out, int64_t K,
                               bool f32, cudaStream_t s);
+int64_t rmsnorm_bwd_chunks(int64_t M);
+cudaError_t launch_rmsnorm_backward(const void* dY, const void* H, const float* r, const float* gamma,
+                                    const float* S, int T, const void* dH_in, void* dH, void* Yt, float* dgamma,
+                                    float* part, int64_t M, int64_t N, cudaStream_t s);
 cudaError_t launch_amax(const void* x, int64_t n, bool f32, float* amax, cudaStream_t s);
 cudaError_t launch_quantize_e4m3(const void* x, int64_t n, bool f32, const float* amax, uint8_t* q,
                                  float* scale, cudaStream_t s);

@@ -71,13 +71,27 @@ __device__ unsigned g_status;
 
 constexpr int kNoPhase = -1;
 
-template <int KIND, int EPI_A, int EPI_B, int STAGES_, int NSLOTS_, int CG_ = 1>
+// Programs whose B tile is gate rows ++ up rows (N = 128 + 128).
+__host__ __device__ constexpr bool is_swiglu(int epi) { return epi == kEpiSwiGLU || epi == kEpiSwiGLUSave; }
+
+template <int KIND, int EPI_A, int EPI_B, int STAGES_, int NSLOTS_, int CG_ = 1, bool A_MN_ = false,
+          bool B_MN_ = false>
 struct GemmCfg {
   static constexpr int kKind = KIND;
+  // MN-major operands: A stored [K, M] (m contiguous) / B stored [K, N], loaded
+  // as 64-element-wide TMA boxes of BK k-rows each
+  static constexpr bool A_MN = A_MN_;
+  static constexpr bool B_MN = B_MN_;
   static constexpr int kEpiA = EPI_A;         // program of the (first) phase
   static constexpr int kEpiB = EPI_B;         // program of the second phase, or kNoPhase
   static constexpr bool TWO_PHASE = EPI_B != kNoPhase;
-  static constexpr bool HAS_LOADER = EPI_A == kEpiResidualPartialRms;  // warp 6 owns the slot ring
+  // warp 6 owns the slot ring: programs that read a tile of another tensor
+  static constexpr bool HAS_LOADER =
+      EPI_A == kEpiResidualPartialRms || EPI_A == kEpiGradNorm || EPI_A == kEpiSwiGLUBwd;
+  // slots one output box occupies: SwiGLU backward reads G and U and writes dG and dU
+  __host__ __device__ static constexpr int slots_per_box(int epi) {
+    return epi == kEpiSwiGLUBwd ? 2 : (epi == kEpiSwiGLUSave ? 3 : 1);
+  }
   static constexpr int CG = CG_;              // CTAs per MMA (cta_group::1 or ::2)
   static constexpr int BM = 128;              // accumulator rows per CTA
   static constexpr int TILE_M = BM * CG;      // output rows per tile (per CTA pair)
@@ -93,10 +107,10 @@ struct GemmCfg {
   static constexpr int B_BYTES = B_ROWS * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // this CTA's bytes per stage
   // output columns per tile of a program
-  __host__ __device__ static constexpr int out_cols(int epi) { return epi == kEpiSwiGLU ? BN / 2 : BN; }
+  __host__ __device__ static constexpr int out_cols(int epi) { return is_swiglu(epi) ? BN / 2 : BN; }
   // rows of one B TMA box: SwiGLU with one CTA loads gate and up halves
   // separately; with a pair, each CTA loads one of them whole
-  __host__ __device__ static constexpr int b_box_rows(int epi) { return (epi == kEpiSwiGLU && CG == 1) ? BN / 2 : B_ROWS; }
+  __host__ __device__ static constexpr int b_box_rows(int epi) { return (is_swiglu(epi) && CG == 1) ? BN / 2 : B_ROWS; }
   static constexpr int OUT_ELEM = KIND == kKindTF32 ? 4 : 2;  // fp32 out for tf32, else bf16
   static constexpr int BOX_COLS = 128 / OUT_ELEM;             // output columns per 128-byte box
   static constexpr int NC32 = BOX_COLS / 32;  // 32-column TMEM loads per box (per operand half)
@@ -113,6 +127,7 @@ struct GemmCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * NSLOTS + 1;
   static constexpr int SMEM_BYTES = OFF_BARS + NUM_BARS * 8 + 16 + 1024;  // + slack for 1 KB alignment
   static_assert(CG == 1 || CG == 2, "CTA group");
+  static_assert(NSLOTS >= 2 * slots_per_box(EPI_A) || HAS_LOADER, "output staging needs two boxes of slots");
   static_assert(!TWO_PHASE || (EPI_A == kEpiResidualPartialRms && (EPI_B == kEpiRowScale || EPI_B == kEpiSwiGLU)),
                 "a two-phase launch is residual GEMM -> row-scale or SwiGLU GEMM");
   static_assert(TMEM_COLS == 512, "two 256-column accumulators");
@@ -121,7 +136,12 @@ struct GemmCfg {
   static_assert(NSLOTS >= 2, "slot ring");
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory");
   static constexpr uint32_t FMT = KIND == kKindBF16 ? 1u : (KIND == kKindTF32 ? 2u : 0u);
-  static constexpr uint32_t IDESC = make_idesc(FMT, FMT, TILE_M, BN);
+  static constexpr int MN_BOX = 64;                  // MN elements per MN-major box (128 bytes of bf16)
+  static constexpr int MN_BOX_BYTES = MN_BOX * 128;  // BK k-rows of 128 bytes
+  static_assert(!(A_MN || B_MN) || (KIND == kKindBF16 && !TWO_PHASE), "MN-major operands: bf16, one phase");
+  static_assert((EPI_A != kEpiGradNorm && EPI_A != kEpiSwiGLUBwd) || (KIND == kKindBF16 && NSLOTS % 2 == 0),
+                "backward programs: bf16, an even slot ring");
+  static constexpr uint32_t IDESC = make_idesc(FMT, FMT, TILE_M, BN, A_MN, B_MN);
 };
 
 struct TileCoord {
@@ -285,7 +305,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if constexpr (C::kEpiA == kEpiSwiGLU) tma_prefetch_desc(&tmB2);
+    if constexpr (is_swiglu(C::kEpiA)) tma_prefetch_desc(&tmB2);
+    if constexpr (C::kEpiA == kEpiSwiGLUSave) tma_prefetch_desc(&tmD_b);
     if constexpr (C::HAS_LOADER) tma_prefetch_desc(&tmR);
     tma_prefetch_desc(&tmD);
     if constexpr (C::TWO_PHASE) {
@@ -325,7 +346,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const CUtensorMap* mA = pB ? &tmA_b : &tmA;
         const CUtensorMap* mB = pB ? &tmB_b : &tmB;
         const CUtensorMap* mB2 = pB ? &tmB2_b : &tmB2;
-        const bool swiglu = pB ? C::kEpiB == kEpiSwiGLU : C::kEpiA == kEpiSwiGLU;
+        const bool swiglu = pB ? is_swiglu(C::kEpiB) : is_swiglu(C::kEpiA);
         const int num_kb = ((pB ? pb.K : pa.K) + C::BK - 1) / C::BK;
         const int a_row = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
         if (pB) {
@@ -341,7 +362,29 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           const int kx = kb * C::BK;
           uint8_t* a = sA + stage * C::A_BYTES;
           uint8_t* b = sB + stage * C::B_BYTES;
-          if constexpr (C::CG == 1) {
+          if constexpr (C::A_MN || C::B_MN) {
+            // MN-major boxes: x = MN coordinate, y = k
+            if constexpr (C::CG == 1) mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            else if (mma_cta) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+            const uint32_t fb = C::CG == 2 ? full0 + static_cast<uint32_t>(stage) * 8u : 0u;
+            auto load = [&](void* dst, const CUtensorMap* m, int x, int y, uint64_t pol) {
+              if constexpr (C::CG == 1) tma_load_2d(dst, m, &full[stage], x, y, pol);
+              else tma_load_2d_pair(dst, m, fb, x, y, pol);
+            };
+            if constexpr (C::A_MN) {
+#pragma unroll
+              for (int i = 0; i < C::BM / C::MN_BOX; ++i) load(a + i * C::MN_BOX_BYTES, mA, a_row + i * C::MN_BOX, kx, pol_a);
+            } else {
+              load(a, mA, kx, a_row, pol_a);
+            }
+            const int b_row = tl.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS;
+            if constexpr (C::B_MN) {
+#pragma unroll
+              for (int i = 0; i < C::B_ROWS / C::MN_BOX; ++i) load(b + i * C::MN_BOX_BYTES, mB, b_row + i * C::MN_BOX, kx, pol_b);
+            } else {
+              load(b, mB, kx, b_row, pol_b);
+            }
+          } else if constexpr (C::CG == 1) {
             mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
             tma_load_2d(a, mA, &full[stage], kx, a_row, pol_a);
             if (swiglu) {
@@ -393,14 +436,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + stage * C::A_BYTES));
-          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(sB + stage * C::B_BYTES));
+          const uint32_t a_s = smem_u32(sA + stage * C::A_BYTES), b_s = smem_u32(sB + stage * C::B_BYTES);
+          const uint64_t adesc = C::A_MN ? sdesc_mnmajor_sw128(a_s, C::MN_BOX_BYTES) : sdesc_kmajor_sw128(a_s);
+          const uint64_t bdesc = C::B_MN ? sdesc_mnmajor_sw128(b_s, C::MN_BOX_BYTES) : sdesc_kmajor_sw128(b_s);
+          // one MMA step along K: 32 bytes inside a K-major swizzle row (+2 in
+          // the descriptor's 16-byte units), or UMMA_K rows of 128 bytes of an
+          // MN-major tile (+UMMA_K * 8)
+          constexpr uint64_t a_step = C::A_MN ? C::UMMA_K * 8u : 2u;
+          constexpr uint64_t b_step = C::B_MN ? C::UMMA_K * 8u : 2u;
 #pragma unroll
-          for (int k = 0; k < C::K_STEPS; ++k) {
-            // 32 bytes further along K inside the swizzle atom = +2 in the
-            // descriptor's 16-byte address units
-            tc_mma<C::kKind, C::CG>(d_tmem, adesc + 2u * k, bdesc + 2u * k, C::IDESC, (kb | k) != 0);
-          }
+          for (int k = 0; k < C::K_STEPS; ++k)
+            tc_mma<C::kKind, C::CG>(d_tmem, adesc + a_step * k, bdesc + b_step * k, C::IDESC, (kb | k) != 0);
           tc_commit<C::CG>(&empty[stage], kPair);  // both CTAs' stage is free again
           if (++stage == C::STAGES) {
             stage = 0;
@@ -430,23 +476,26 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           if (row0 >= M) continue;  // this CTA's half of the tile is empty
           const int oc = pB ? C::out_cols(C::kEpiB) : C::out_cols(C::kEpiA);
           const int n_out = pB ? pb.N_out : pa.N_out;
-          for (int b = 0; b < oc / C::BOX_COLS; ++b) {
+          for (int b = 0; b < oc / C::BOX_COLS && ok; ++b) {
             const int col0 = tl.n * oc + b * C::BOX_COLS;
             if (col0 >= n_out) break;
-            if (!mbar_wait(&r_empty[slot], phase ^ 1u, abort_flag, &g_status)) {
-              ok = false;
-              break;
-            }
-            if (pB) {
-              mbar_arrive(&r_full[slot]);
-            } else {
-              mbar_arrive_expect_tx(&r_full[slot], C::SLOT_BYTES);
-              tma_load_2d(slots + slot * C::SLOT_BYTES, &tmR, &r_full[slot], col0, row0, pol);
-            }
-            ++used;
-            if (++slot == C::NSLOTS) {
-              slot = 0;
-              phase ^= 1u;
+            // SwiGLU backward: G's box, then U's box gu_off columns further
+            for (int sb = 0; sb < C::slots_per_box(C::kEpiA); ++sb) {
+              if (!mbar_wait(&r_empty[slot], phase ^ 1u, abort_flag, &g_status)) {
+                ok = false;
+                break;
+              }
+              if (pB) {
+                mbar_arrive(&r_full[slot]);
+              } else {
+                mbar_arrive_expect_tx(&r_full[slot], C::SLOT_BYTES);
+                tma_load_2d(slots + slot * C::SLOT_BYTES, &tmR, &r_full[slot], col0 + sb * pa.ep.gu_off, row0, pol);
+              }
+              ++used;
+              if (++slot == C::NSLOTS) {
+                slot = 0;
+                phase ^= 1u;
+              }
             }
           }
         }
@@ -477,7 +526,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       float sab = 1.0f, sab2 = 1.0f;
       if constexpr (C::kKind == kKindE4M3) {
         sab = *ep.scale_a * *ep.scale_b;
-        if constexpr (EPI == kEpiSwiGLU) sab2 = *ep.scale_a * *ep.scale_b2;
+        if constexpr (is_swiglu(EPI)) sab2 = *ep.scale_a * *ep.scale_b2;
       }
       const int row0 = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
       const int row = row0 + row_in_tile;
@@ -526,37 +575,67 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const int col0 = tl.n * OUT_COLS + b * C::BOX_COLS;
         if (col0 >= N_out) break;  // uniform over the CTA
         uint32_t g[C::NC32][32];
-        uint32_t u[EPI == kEpiSwiGLU ? C::NC32 : 1][32];
+        uint32_t u[is_swiglu(EPI) ? C::NC32 : 1][32];
 #pragma unroll
         for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + b * C::BOX_COLS + 32 * i, g[i]);
-        if constexpr (EPI == kEpiSwiGLU) {
+        if constexpr (is_swiglu(EPI)) {
 #pragma unroll
           for (int i = 0; i < C::NC32; ++i) tmem_ld32(t_row + C::BN / 2 + b * C::BOX_COLS + 32 * i, u[i]);
         }
         tmem_wait_ld(g[0]);
 #pragma unroll
         for (int i = 1; i < C::NC32; ++i) tmem_touch(g[i]);
-        if constexpr (EPI == kEpiSwiGLU) {
+        if constexpr (is_swiglu(EPI)) {
 #pragma unroll
           for (int i = 0; i < C::NC32; ++i) tmem_touch(u[i]);
         }
         if (b == NUM_BOXES - 1 || col0 + C::BOX_COLS >= N_out) release_acc();
+        constexpr int SPB = C::slots_per_box(EPI);
         bool got = true;
-        if constexpr (C::HAS_LOADER) got = mbar_wait(&r_full[slot], sphase, abort_flag, &g_status);
+        if constexpr (C::HAS_LOADER) {
+#pragma unroll
+          for (int sb = 0; sb < SPB; ++sb) got = got && mbar_wait(&r_full[slot + sb], sphase, abort_flag, &g_status);
+        }
         uint8_t* sp = slots + slot * C::SLOT_BYTES;
+        uint8_t* sp2 = sp + (SPB - 1) * C::SLOT_BYTES;  // SwiGLU backward: U in, dU out
         if (got) {
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             float o[C::CHUNK_COLS];
+            float gs[EPI == kEpiSwiGLUSave ? C::CHUNK_COLS : 1], us[EPI == kEpiSwiGLUSave ? C::CHUNK_COLS : 1];
 #pragma unroll
             for (int e = 0; e < C::CHUNK_COLS; ++e) {
               const int j = c * C::CHUNK_COLS + e;
               const float a = __uint_as_float(g[j >> 5][j & 31]);
-              if constexpr (EPI == kEpiSwiGLU) {
+              if constexpr (is_swiglu(EPI)) {
                 const float uu = __uint_as_float(u[j >> 5][j & 31]);
-                o[e] = silu_f(a * sg) * (uu * su);
+                const float G = a * sg, U = uu * su;
+                o[e] = silu_f(G) * U;
+                if constexpr (EPI == kEpiSwiGLUSave) {
+                  gs[e] = G;
+                  us[e] = U;
+                }
               } else {
                 o[e] = a * sg;
+              }
+            }
+            if constexpr (EPI == kEpiSwiGLUSave) {
+              // the pre-activations, for the backward: G to the second slot, U to the third
+              uint32_t wg[4], wu[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                wg[e] = pack_bf16x2(gs[2 * e], gs[2 * e + 1]);
+                wu[e] = pack_bf16x2(us[2 * e], us[2 * e + 1]);
+              }
+              *reinterpret_cast<uint4*>(sp + C::SLOT_BYTES + swz(row_in_tile, c)) = make_uint4(wg[0], wg[1], wg[2], wg[3]);
+              *reinterpret_cast<uint4*>(sp + 2 * C::SLOT_BYTES + swz(row_in_tile, c)) =
+                  make_uint4(wu[0], wu[1], wu[2], wu[3]);
+            }
+            if constexpr (EPI == kEpiRowScale) {
+              if (ep.col_scale != nullptr) {  // diag(col_scale) on the right
+                const int col = col0 + c * C::CHUNK_COLS;
+#pragma unroll
+                for (int e = 0; e < C::CHUNK_COLS; ++e) o[e] *= col + e < N_out ? __ldg(ep.col_scale + col + e) : 0.0f;
               }
             }
             if constexpr (EPI == kEpiRowScale) {
@@ -576,7 +655,44 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               }
             }
             void* p = sp + swz(row_in_tile, c);
-            if constexpr (C::OUT_ELEM == 2) {
+            if constexpr (C::OUT_ELEM == 2 && EPI == kEpiGradNorm) {
+              // stored dY, and sum_j gamma_j dY_j H_j over the stored values
+              const uint4 hv = *reinterpret_cast<const uint4*>(p);
+              const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+              const int col = col0 + c * C::CHUNK_COLS;
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                w[e] = pack_bf16x2(o[2 * e], o[2 * e + 1]);
+                const float g0 = col + 2 * e < N_out ? __ldg(ep.col_scale + col + 2 * e) : 0.0f;
+                const float g1 = col + 2 * e + 1 < N_out ? __ldg(ep.col_scale + col + 2 * e + 1) : 0.0f;
+                ss += g0 * bf16_lo(w[e]) * bf16_lo(hw[e]) + g1 * bf16_hi(w[e]) * bf16_hi(hw[e]);
+              }
+              *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else if constexpr (C::OUT_ELEM == 2 && EPI == kEpiSwiGLUBwd) {
+              // act = silu(G) U: dG = dAct U sigmoid(G) (1 + G (1 - sigmoid(G))), dU = dAct G sigmoid(G)
+              void* p2 = sp2 + swz(row_in_tile, c);
+              const uint4 gv = *reinterpret_cast<const uint4*>(p), uv = *reinterpret_cast<const uint4*>(p2);
+              const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+              uint32_t wg[4], wu[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float dg[2], du[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const float G = h ? bf16_hi(gw[e]) : bf16_lo(gw[e]);
+                  const float U = h ? bf16_hi(uw[e]) : bf16_lo(uw[e]);
+                  const float sgm = __fdividef(1.0f, 1.0f + __expf(-G));
+                  const float da = o[2 * e + h];
+                  dg[h] = da * U * sgm * (1.0f + G * (1.0f - sgm));
+                  du[h] = da * G * sgm;
+                }
+                wg[e] = pack_bf16x2(dg[0], dg[1]);
+                wu[e] = pack_bf16x2(du[0], du[1]);
+              }
+              *reinterpret_cast<uint4*>(p) = make_uint4(wg[0], wg[1], wg[2], wg[3]);
+              *reinterpret_cast<uint4*>(p2) = make_uint4(wu[0], wu[1], wu[2], wu[3]);
+            } else if constexpr (C::OUT_ELEM == 2) {
               uint32_t w[4];
               if constexpr (EPI == kEpiResidualPartialRms) {
                 const uint4 rv = *reinterpret_cast<const uint4*>(p);
@@ -611,7 +727,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               *reinterpret_cast<float4*>(p) = v;
             }
           }
-          if constexpr (EPI == kEpiResidualPartialRms) {
+          if constexpr (EPI == kEpiResidualPartialRms || EPI == kEpiGradNorm) {
             const int gcol = col0 + C::BOX_COLS;  // end column of this box
             if (gcol % kPartialCols == 0 || gcol >= N_out) {
               if (row < M) ep.P[static_cast<int64_t>(row) * ep.T + col0 / kPartialCols] = ss;
@@ -628,11 +744,20 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         if (leader) {
           tma_store_2d(mD, sp, col0, row0);
+          if constexpr (EPI == kEpiSwiGLUBwd) tma_store_2d(mD, sp2, col0 + ep.gu_off, row0);
+          if constexpr (EPI == kEpiSwiGLUSave) {
+            tma_store_2d(&tmD_b, sp + C::SLOT_BYTES, col0, row0);
+            tma_store_2d(&tmD_b, sp + 2 * C::SLOT_BYTES, col0 + ep.gu_off, row0);
+          }
           tma_store_commit();
-          tma_store_wait_read_all();  // slot readable again before anyone rewrites it
-          if constexpr (C::HAS_LOADER) mbar_arrive(&r_empty[slot]);
+          tma_store_wait_read_all();  // slots readable again before anyone rewrites them
+          if constexpr (C::HAS_LOADER) {
+#pragma unroll
+            for (int sb = 0; sb < SPB; ++sb) mbar_arrive(&r_empty[slot + sb]);
+          }
         }
-        if (++slot == C::NSLOTS) {
+        slot += SPB;
+        if (slot == C::NSLOTS) {
           slot = 0;
           sphase ^= 1u;
         }
@@ -709,21 +834,41 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
     const uint64_t kbytes = static_cast<uint64_t>(K) * C::ELEM;
     const uint64_t obytes = static_cast<uint64_t>(N_out) * C::OUT_ELEM;
     const uint32_t brows = static_cast<uint32_t>(C::b_box_rows(epi));
-    CUresult e = encode_tmap_2d(a, in_dt, A, K, p.M, kbytes, C::BK, C::BM);
-    if (e == CUDA_SUCCESS) e = encode_tmap_2d(b, in_dt, B, K, N_out, kbytes, C::BK, brows);
-    if (e == CUDA_SUCCESS) e = encode_tmap_2d(b2, in_dt, B2 ? B2 : B, K, N_out, kbytes, C::BK, brows);
+    CUresult e = C::A_MN ? encode_tmap_2d(a, in_dt, A, p.M, K, static_cast<uint64_t>(p.M) * C::ELEM, C::MN_BOX, C::BK)
+                         : encode_tmap_2d(a, in_dt, A, K, p.M, kbytes, C::BK, C::BM);
+    if (e == CUDA_SUCCESS)
+      e = C::B_MN ? encode_tmap_2d(b, in_dt, B, N_out, K, static_cast<uint64_t>(N_out) * C::ELEM, C::MN_BOX, C::BK)
+                  : encode_tmap_2d(b, in_dt, B, K, N_out, kbytes, C::BK, brows);
+    if (e == CUDA_SUCCESS) {
+      if (C::B_MN || B2 == nullptr)
+        *b2 = *b;  // read only by SwiGLU programs, which have a K-major up weight
+      else
+        e = encode_tmap_2d(b2, in_dt, B2, K, N_out, kbytes, C::BK, brows);
+    }
     if (e == CUDA_SUCCESS) e = encode_tmap_2d(d, out_dt, D, N_out, p.M, obytes, C::BOX_COLS, C::BM);
     return e;
   };
   CUresult e = encode_phase(&tmA, &tmB, &tmB2, &tmD, p.A, p.B, p.B2, p.D, p.N_out, p.K, C::kEpiA);
+  // SwiGLU backward reads G || U and writes dG || dU: [M, 2 N_out] tensors
+  const uint64_t rd_cols = static_cast<uint64_t>(p.N_out) * (C::kEpiA == kEpiSwiGLUBwd ? 2 : 1);
   if (e == CUDA_SUCCESS)
-    e = encode_tmap_2d(&tmR, out_dt, C::HAS_LOADER ? p.R : p.D, p.N_out, p.M,
-                       static_cast<uint64_t>(p.N_out) * C::OUT_ELEM, C::BOX_COLS, C::BM);
+    e = encode_tmap_2d(&tmR, out_dt, C::HAS_LOADER ? p.R : p.D, rd_cols, p.M, rd_cols * C::OUT_ELEM, C::BOX_COLS,
+                       C::BM);
+  if (e == CUDA_SUCCESS && C::kEpiA == kEpiSwiGLUBwd)
+    e = encode_tmap_2d(&tmD, out_dt, p.D, rd_cols, p.M, rd_cols * C::OUT_ELEM, C::BOX_COLS, C::BM);
+  const uint64_t gu_cols = 2 * static_cast<uint64_t>(p.N_out);  // SwiGLU save: G || U [M, 2 N_out]
   if (e == CUDA_SUCCESS) {
-    if constexpr (C::TWO_PHASE)
+    if constexpr (C::TWO_PHASE) {
       e = encode_phase(&tmA_b, &tmB_b, &tmB2_b, &tmD_b, p.b.A, p.b.B, p.b.B2, p.b.D, p.b.N_out, p.b.K, C::kEpiB);
-    else
-      tmA_b = tmA, tmB_b = tmB, tmB2_b = tmB2, tmD_b = tmD;  // unused by a one-phase launch
+    } else {
+      // unused by a one-phase launch, except that SwiGLU save stores G || U through tmD_b
+      tmA_b = tmA;
+      tmB_b = tmB;
+      tmB2_b = tmB2;
+      tmD_b = tmD;
+      if constexpr (C::kEpiA == kEpiSwiGLUSave)
+        e = encode_tmap_2d(&tmD_b, out_dt, p.GU, gu_cols, p.M, gu_cols * C::OUT_ELEM, C::BOX_COLS, C::BM);
+    }
   }
   if (e != CUDA_SUCCESS) {
     *msg = "cuTensorMapEncodeTiled rejected an operand (pointer, stride or extent)";
@@ -793,7 +938,7 @@ inline int choose_cta_group(const GemmProblem& p) {
     if (f[0] == '1') return 1;
     if (f[0] == '2') return 2;
   }
-  const int out_cols = p.epi == kEpiSwiGLU ? 128 : 256;
+  const int out_cols = is_swiglu(p.epi) ? 128 : 256;
   const long tiles2 = static_cast<long>((p.M + 255) / 256) * ((p.N_out + out_cols - 1) / out_cols);
   return tiles2 >= device_sm_count() / 2 ? 2 : 1;
 }
@@ -805,6 +950,40 @@ inline int choose_cta_group(const GemmProblem& p) {
 template <int KIND>
 cudaError_t launch_gemm(const GemmProblem& p, const char** msg) {
   const bool pair = choose_cta_group(p) == 2;
+  if constexpr (KIND == kKindBF16) {
+    // backward programs: dY = dOut . W (W's forward W^T read MN-major)
+    if (p.epi == kEpiGradNorm || p.epi == kEpiSwiGLUBwd) {
+      if (!p.b_mn || p.a_mn) {
+        *msg = "backward programs take a K-major A and an MN-major B";
+        return cudaErrorInvalidValue;
+      }
+      if (p.epi == kEpiGradNorm)
+        return pair ? launch_cfg<GemmCfg<KIND, kEpiGradNorm, kNoPhase, 5, 4, 2, false, true>>(p, msg)
+                    : launch_cfg<GemmCfg<KIND, kEpiGradNorm, kNoPhase, 3, 4, 1, false, true>>(p, msg);
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiSwiGLUBwd, kNoPhase, 5, 4, 2, false, true>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiSwiGLUBwd, kNoPhase, 3, 4, 1, false, true>>(p, msg);
+    }
+    // MN-major operands (transposed products of the backward pass): row-scale program
+    if (p.a_mn || p.b_mn) {
+      if (p.epi != kEpiRowScale || p.b.epi != -1) {
+        *msg = "MN-major operands take the row-scale program only";
+        return cudaErrorInvalidValue;
+      }
+      if (p.a_mn && p.b_mn)
+        return pair ? launch_cfg<GemmCfg<KIND, kEpiRowScale, kNoPhase, 6, 2, 2, true, true>>(p, msg)
+                    : launch_cfg<GemmCfg<KIND, kEpiRowScale, kNoPhase, 4, 2, 1, true, true>>(p, msg);
+      if (p.b_mn)
+        return pair ? launch_cfg<GemmCfg<KIND, kEpiRowScale, kNoPhase, 6, 2, 2, false, true>>(p, msg)
+                    : launch_cfg<GemmCfg<KIND, kEpiRowScale, kNoPhase, 4, 2, 1, false, true>>(p, msg);
+      *msg = "an MN-major A needs an MN-major B";
+      return cudaErrorInvalidValue;
+    }
+  } else {
+    if (p.a_mn || p.b_mn) {
+      *msg = "MN-major operands are bf16 only";
+      return cudaErrorInvalidValue;
+    }
+  }
   if (p.b.epi == kEpiRowScale)
     return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 5, 4, 2>>(p, msg)
                 : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 3, 4, 1>>(p, msg);
@@ -821,6 +1000,12 @@ cudaError_t launch_gemm(const GemmProblem& p, const char** msg) {
     case kEpiSwiGLU:
       return pair ? launch_cfg<GemmCfg<KIND, kEpiSwiGLU, kNoPhase, 6, 2, 2>>(p, msg)
                   : launch_cfg<GemmCfg<KIND, kEpiSwiGLU, kNoPhase, 4, 2, 1>>(p, msg);
+    case kEpiSwiGLUSave:
+      if constexpr (KIND == kKindBF16)
+        return pair ? launch_cfg<GemmCfg<KIND, kEpiSwiGLUSave, kNoPhase, 4, 6, 2>>(p, msg)
+                    : launch_cfg<GemmCfg<KIND, kEpiSwiGLUSave, kNoPhase, 2, 6, 1>>(p, msg);
+      *msg = "saving the SwiGLU pre-activations is bf16 only";
+      return cudaErrorInvalidValue;
     default:
       *msg = "unknown epilogue program";
       return cudaErrorInvalidValue;

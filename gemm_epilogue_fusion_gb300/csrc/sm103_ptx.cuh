@@ -285,12 +285,32 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor: fp32 accumulator (bits 4-5 = 1), A and B K-major,
-// shape M x N (N >> 3 at bits 17-22, M >> 4 at bits 24-28).
+// Shared-memory matrix descriptor for an MN-major operand tile laid out by
+// TMA with 128-byte swizzling: each 128-byte row holds 64 consecutive MN
+// elements (bf16) of one k; 8 k-rows form a 1024-byte swizzle atom, atoms
+// follow each other along K every 1024 bytes (stride byte offset), and the
+// next 64 MN elements start `mn_stride` bytes further, one TMA box (leading
+// byte offset).  The opposite assignment of the two offsets gives wrong
+// products; both were tried against a float64 reference.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: next 64 MN elements
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;                  // stride byte offset: next 8 k-rows
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor: fp32 accumulator (bits 4-5 = 1), shape M x N
+// (N >> 3 at bits 17-22, M >> 4 at bits 24-28); A / B K-major unless
+// a_mn / b_mn set bit 15 / 16 (MN-major).
 // Operand formats (bits 7-9 and 10-12): kind::f16 -> 1 = bf16; kind::tf32 ->
 // 2 = tf32; kind::f8f6f4 -> 0 = e4m3.
-__host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t m, uint32_t n) {
-  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t m, uint32_t n,
+                                                  bool a_mn = false, bool b_mn = false) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 enum MmaKind { kKindBF16 = 0, kKindTF32 = 1, kKindE4M3 = 2 };

@@ -79,6 +79,11 @@ typedef enum {
 
 typedef enum { CODA_F32 = 0, CODA_BF16 = 1, CODA_E4M3 = 2 } coda_dtype;
 
+/* Storage of a GEMM operand: CODA_K_MAJOR = rows of the output dimension
+ * with K contiguous ([M, K] / [N, K]); CODA_MN_MAJOR = rows of K with the
+ * output dimension contiguous ([K, M] / [K, N], i.e. the transpose). */
+typedef enum { CODA_K_MAJOR = 0, CODA_MN_MAJOR = 1 } coda_layout;
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 CODA_API int coda_version(void);
 
@@ -248,6 +253,78 @@ CODA_API coda_status coda_block_swiglu_noalloc(const void* X, const void* W1t, c
                                                const void* Wut, float eps, void* H, float* P, float* r_out,
                                                void* Act, int64_t M, int64_t N, int64_t K, int64_t I,
                                                coda_dtype dtype, cudaStream_t stream);
+
+/* General GEMM on the same tcgen05 kernels, for the transposed products of
+ * the block's backward pass (dX = dh . W1, dW = X^T . dh, ...):
+ *   D[m, n] = row_scale[m] * col_scale[n] * sum_k A(m, k) B(n, k)
+ *   A(m, k) = A[m*K + k] (CODA_K_MAJOR) or A[k*M + m] (CODA_MN_MAJOR)
+ *   B(n, k) = B[n*K + k] (CODA_K_MAJOR) or B[k*N + n] (CODA_MN_MAJOR)
+ * row_scale [M], col_scale [N]: nullable fp32 (= 1).  D [M, N] in the output
+ * type of dtype (fp32 for CODA_F32, else bf16).  dtype CODA_F32 or
+ * CODA_BF16; MN-major operands are bf16 only, and an MN-major A needs an
+ * MN-major B.  Every stored row must be a multiple of 16 bytes. */
+CODA_API coda_status coda_gemm(const void* A, coda_layout a_layout, const void* B, coda_layout b_layout, void* D,
+                               int64_t M, int64_t N, int64_t K, coda_dtype dtype, const float* row_scale,
+                               const float* col_scale, cudaStream_t stream);
+
+/* ---- Backward of the block (the CODA write-up, section "CODA: the treasure
+ * hidden in the epilogue": when the forward epilogue is block-local the
+ * backward inherits the same GEMM + epilogue structure).  bf16 only.
+ * Forward being differentiated: h = R + X W1, r_i = 1/sqrt(mean_j h_ij^2 + eps),
+ * y = h r gamma, then Z = y W2 or act = silu(y Wg) (y Wu).  Gradients:
+ *   dy     = dZ . W2                    coda_gemm_grad_norm (also S)
+ *   dh     = r gamma dy - h r^3/N sum_j gamma_j dy_j h_j (+ dH_in)
+ *   dgamma = sum_i dy h r,  Yt = r h    coda_rmsnorm_backward
+ *   dX = dh . W1^T, dW1 = X^T dh, dW2 = (Yt^T dZ) diag(gamma)   coda_gemm
+ *   SwiGLU: dAct = dOut . Wd, dG = dAct U silu'(G), dU = dAct silu(G)
+ *                                       coda_gemm_swiglu_backward
+ */
+
+/* dY = dOut . Wt with the row reduction of RMSNorm's backward in the epilogue:
+ *   dY[i, j] = sum_k dOut[i, k] Wt[k, j]        (Wt [K, N]: the forward weight
+ *                                                as stored, W^T of its GEMM)
+ *   S[i, g]  = sum over j in [128 g, 128 g + 128) of gamma_j dY_ij H_ij
+ *              (of the stored, rounded dY; H [M, N] is the forward's h)
+ *   dOut [M, K], dY [M, N] bf16; gamma [N] fp32; S [M, coda_partial_cols(N)] fp32.
+ * For the SwiGLU block, dOut = dG || dU [M, 2I] and Wt = Wg^T || Wu^T stacked
+ * as [2I, N] (the forward's Wgt above Wut, unfolded). */
+CODA_API coda_status coda_gemm_grad_norm(const void* dOut, const void* Wt, const void* H, const float* gamma,
+                                         void* dY, float* S, int64_t M, int64_t N, int64_t K, coda_dtype dtype,
+                                         cudaStream_t stream);
+
+/* Elementwise RMSNorm backward from coda_gemm_grad_norm's dY and S:
+ *   c_i = r_i^3 / N * sum_g S[i, g];  dH = r gamma dY - c H (+ dH_in);
+ *   Yt = r H (the operand of the weight gradient);  dgamma_j = sum_i dY H r.
+ * dY, H, dH_in (nullable), dH, Yt: [M, N] bf16; r [M], gamma [N], dgamma [N]
+ * fp32.  workspace: coda_rmsnorm_backward_workspace_bytes(M, N) bytes of
+ * device memory (dgamma partials, summed in a fixed order: deterministic).
+ * N a multiple of 8. */
+CODA_API int64_t coda_rmsnorm_backward_workspace_bytes(int64_t M, int64_t N);
+CODA_API coda_status coda_rmsnorm_backward(const void* dY, const void* H, const float* r, const float* gamma,
+                                           const float* S, const void* dH_in, void* dH, void* Yt, float* dgamma,
+                                           float* workspace, int64_t M, int64_t N, cudaStream_t stream);
+
+/* The forward SwiGLU GEMM that also saves its pre-activations for the
+ * backward (the "matrix block store" primitive of the write-up's section
+ * "five blocks and a Lego language"): as coda_gemm_swiglu (r given) or
+ * coda_gemm_swiglu_fused_rms (P, eps, r_out), exactly one of r and P, plus
+ *   GU [M, 2I] bf16: G = r (H Wgt^T) in columns [0, I), U = r (H Wut^T) in [I, 2I).
+ * bf16 only; I a multiple of 64 (the G half is stored in 64-column boxes that
+ * must not reach into the U half). */
+CODA_API coda_status coda_gemm_swiglu_save(const void* H, const void* Wgt, const void* Wut, const float* r,
+                                           const float* P, float eps, float* r_out, void* Act, void* GU, int64_t M,
+                                           int64_t I, int64_t K, coda_dtype dtype, cudaStream_t stream);
+
+/* SwiGLU backward in the epilogue of the GEMM that produces its upstream
+ * gradient (the down projection's dAct = dOut . Wd):
+ *   dAct[i, n] = sum_k dOut[i, k] Wt[k, n]    (Wt [K, I]: the down weight as stored)
+ *   dG = dAct U silu'(G),  dU = dAct silu(G),  silu'(x) = s(x) (1 + x (1 - s(x)))
+ * GU [M, 2I]: the forward's pre-activations G || U (saved by
+ * coda_gemm_swiglu_save); dGU [M, 2I] receives dG || dU.  dAct itself never
+ * reaches memory.  I a multiple of 64. */
+CODA_API coda_status coda_gemm_swiglu_backward(const void* dOut, const void* Wt, const void* GU, void* dGU,
+                                               int64_t M, int64_t I, int64_t K, coda_dtype dtype,
+                                               cudaStream_t stream);
 
 /* Per-tensor absolute maximum: *amax = max_i |x_i| over n elements of
  * dtype CODA_F32 or CODA_BF16 (overwritten).  n may be 0 (amax = 0).

@@ -117,3 +117,12 @@ def test_block_calls_validate(lib):
     assert lib.coda_block_rowscale(*args, 1, A + 256 * MB, None) == g.CODA_ERR_INVALID_ARG  # workspace inside h
     assert lib.coda_block_workspace_bytes(8192) == (64 + 1) * 4
     assert lib.coda_block_workspace_bytes(1) == 8
+
+
+def test_swiglu_save_and_backward_need_64_column_halves(lib):
+    B = A + 512 * MB
+    assert lib.coda_gemm_swiglu_save(A, A + 64 * MB, A + 128 * MB, A + 192 * MB, None, 0.0, None, A + 256 * MB,
+                                     A + 320 * MB, 256, 520, 512, 1, None) == g.CODA_ERR_INVALID_ARG
+    assert b"multiple of 64" in lib.coda_last_error()
+    assert lib.coda_gemm_swiglu_backward(A, A + 64 * MB, A + 128 * MB, B, 256, 520, 512, 1, None) \
+        == g.CODA_ERR_INVALID_ARG
