@@ -611,6 +611,122 @@ def profile_one_step(step, rank, what, launches):
         print(json.dumps({"profile_step": what, "launches": launches}), flush=True)
 
 
+def backward_flops(w):
+    """The backward's GEMMs do twice the forward's work (an input and a weight gradient per GEMM)."""
+    return 2.0 * sum(gemm_flops_by_kernel(w).values())
+
+
+def run_coda_backward(args, w):
+    """Backward of the LLaMA block-tail chain from a saved forward state (the
+    forward with coda_gemm_swiglu_save): 12 launches per step."""
+    dist, rank, ws = dist_setup("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import gemm_epilogue_fusion_gb300 as g
+    from gemm_epilogue_fusion_gb300 import chain as C
+    g.load_library()
+    inp = make_inputs(w)
+    sets = []
+    for s in range(2):
+        d = {k: v.to(dev) for k, v in inp.items() if k != "heavy_idx"}
+        gen = torch.Generator(device=dev).manual_seed(100 * rank + s)
+        f = C.fold_weights("full", {k: d[k] for k in d if k.startswith("W")},
+                           {k: d[k] for k in d if k.startswith("gamma")})
+        fwd = C.full_chain_train_forward(d["X"], d["W1t"], d["R"], f["Wgt"], f["Wut"], d["Wdt"], f["Wqt"], w.eps)
+        sets.append({"X": d["X"], "Wot": d["W1t"], "Wgut": torch.cat([d["Wgt"], d["Wut"]], 0).contiguous(),
+                     "Wdt": d["Wdt"], "Wqt": d["Wqt"], "g1": d["gamma1"], "g2": d["gamma2"], "fwd": fwd,
+                     "dZ": torch.randn(w.M, w.N2, generator=gen, device=dev).bfloat16(),
+                     "dH2": torch.randn(w.M, w.N, generator=gen, device=dev).bfloat16(), "f": f, "R": d["R"]})
+    torch.cuda.synchronize()
+
+    def step(st):
+        return C.full_chain_backward(st["X"], st["Wot"], st["Wgut"], st["Wdt"], st["Wqt"], st["g1"], st["g2"],
+                                     st["fwd"], st["dZ"], st["dH2"])
+
+    def fwd_step(st):
+        f = st["f"]
+        C.full_chain_train_forward(st["X"], st["Wot"], st["R"], f["Wgt"], f["Wut"], st["Wdt"], f["Wqt"], w.eps)
+
+    for i in range(args.warmup):
+        step(sets[i % 2])
+    g.coda_get_device_status()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    res = {}
+    with ClockSampler(local) as clk:
+        for name, fn, n in (("backward", step, args.steps), ("train_forward", fwd_step, max(3, args.steps // 2))):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(n):
+                fn(sets[i % 2])
+            b.record()
+            torch.cuda.synchronize()
+            res[name] = a.elapsed_time(b) / 1e3 / n
+    g.coda_get_device_status()
+    if rank != 0:
+        return
+    pk, pk_kind = peaks()
+    bf = backward_flops(w)
+    value = bf * ws / res["backward"] / 1e12
+    print(json.dumps({
+        "metric": METRIC, "pass": "backward", "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["backward"] * 1e3, "higher_is_better": True, "scaling": "weak",
+        "dtype": "bf16", "data": "synthetic", "config": config_of(w, "fused"),
+        "frac_of_peak": value / ws / pk["bf16_tflops"],
+        "train_forward_with_saves": {"value": sum(gemm_flops_by_kernel(w).values()) / res["train_forward"] / 1e12,
+                                     "ms_per_step": res["train_forward"] * 1e3},
+        "gpu_launches": 12 * args.steps, "clocks": clk.summary()}), flush=True)
+
+
+def run_unfused_backward(args, w):
+    """PyTorch eager autograd through the unfused chain (cuBLAS GEMMs, fp32-math
+    RMSNorm, silu * mul), backward only."""
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = make_inputs(w)
+    d = {k: v.to(dev) for k, v in inp.items() if k != "heavy_idx"}
+    P = {k: d[k].clone().requires_grad_(True) for k in ("X", "R", "W1t", "Wgt", "Wut", "Wdt", "Wqt")}
+    G = {k: d[k].clone().requires_grad_(True) for k in ("gamma1", "gamma2")}
+    gen = torch.Generator(device=dev).manual_seed(7)
+    dZ = torch.randn(w.M, w.N2, generator=gen, device=dev).bfloat16()
+    dH2 = torch.randn(w.M, w.N, generator=gen, device=dev).bfloat16()
+
+    def rms(h, gam):
+        hf = h.float()
+        return (hf * torch.rsqrt(hf.pow(2).mean(-1, keepdim=True) + w.eps) * gam).bfloat16()
+
+    def forward():
+        h1 = P["X"] @ P["W1t"].t() + P["R"]
+        y1 = rms(h1, G["gamma1"])
+        act = torch.nn.functional.silu(y1 @ P["Wgt"].t()) * (y1 @ P["Wut"].t())
+        h2 = h1 + act @ P["Wdt"].t()
+        Z = rms(h2, G["gamma2"]) @ P["Wqt"].t()
+        return Z, h2
+
+    def step():
+        Z, h2 = forward()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        torch.autograd.backward([Z, h2], [dZ, dH2])
+        b.record()
+        torch.cuda.synchronize()
+        for t in list(P.values()) + list(G.values()):
+            t.grad = None
+        return a.elapsed_time(b) / 1e3
+
+    for _ in range(args.warmup):
+        step()
+    times = [step() for _ in range(args.steps)]
+    t = statistics.median(times)
+    print(json.dumps({"impl": "unfused_torch_eager_autograd", "pass": "backward", "metric": METRIC,
+                      "value": backward_flops(w) / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
+                      "steps": args.steps, "dtype": "bf16", "config": config_of(w, "separate")}), flush=True)
+
+
 def run_unfused(args, w):
     """cuBLAS + PyTorch eager, unfused: XW, add, RMSNorm (fp32 math), GEMM, silu*mul."""
     if w.chain != "swiglu":
@@ -666,6 +782,8 @@ def main():
     ap.add_argument("--reduce", choices=["block", "fused", "separate"], default="fused",
                     help="block: residual GEMM and consumer in one persistent launch per block; fused: r reduced "
                          "inside the consumer GEMM's epilogue; separate: coda_rms_reduce launch")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
+                    help="backward: gradients of the LLaMA-8B chain from a saved forward state")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
                     help="after warm-up run exactly one step inside cudaProfilerStart/Stop and exit (for ncu)")
@@ -676,7 +794,16 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.pass_ == "backward":
+        if w.chain != "full" or w.dtype != "bf16":
+            ap.error("--pass backward covers the bf16 LLaMA-8B chain (--workload llama8b_chain)")
+        if args.impl == "unfused":
+            run_unfused_backward(args, w)
+        elif args.impl == "coda":
+            run_coda_backward(args, w)
+        else:
+            ap.error("--pass backward has no reference arm")
+    elif args.impl == "reference":
         run_reference(args, w)
     elif args.impl == "unfused":
         run_unfused(args, w)
