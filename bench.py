@@ -698,7 +698,7 @@ def run_unfused_backward(args, w):
         hf = h.float()
         return (hf * torch.rsqrt(hf.pow(2).mean(-1, keepdim=True) + w.eps) * gam).bfloat16()
 
-    def forward():
+    def forward_fn(P, G):
         h1 = P["X"] @ P["W1t"].t() + P["R"]
         y1 = rms(h1, G["gamma1"])
         act = torch.nn.functional.silu(y1 @ P["Wgt"].t()) * (y1 @ P["Wut"].t())
@@ -706,8 +706,10 @@ def run_unfused_backward(args, w):
         Z = rms(h2, G["gamma2"]) @ P["Wqt"].t()
         return Z, h2
 
+    fwd = torch.compile(forward_fn) if args.compile else forward_fn
+
     def step():
-        Z, h2 = forward()
+        Z, h2 = fwd(P, G)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
@@ -722,7 +724,8 @@ def run_unfused_backward(args, w):
         step()
     times = [step() for _ in range(args.steps)]
     t = statistics.median(times)
-    print(json.dumps({"impl": "unfused_torch_eager_autograd", "pass": "backward", "metric": METRIC,
+    print(json.dumps({"impl": "unfused_torch_compile_autograd" if args.compile else "unfused_torch_eager_autograd",
+                      "pass": "backward", "metric": METRIC,
                       "value": backward_flops(w) / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
                       "steps": args.steps, "dtype": "bf16", "config": config_of(w, "separate")}), flush=True)
 
@@ -748,6 +751,9 @@ def run_unfused(args, w):
         g_, u = gu.chunk(2, dim=-1)
         return h, torch.nn.functional.silu(g_) * u
 
+    if args.compile:
+        step = torch.compile(step)
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -763,7 +769,7 @@ def run_unfused(args, w):
     dt = a.elapsed_time(b) / 1e3
     fl = sum(gemm_flops_by_kernel(w).values())
     if rank == 0:
-        print(json.dumps({"impl": "unfused_torch_eager", "metric": METRIC, "value": fl * args.steps / dt / 1e12,
+        print(json.dumps({"impl": "unfused_torch_compile" if args.compile else "unfused_torch_eager", "metric": METRIC, "value": fl * args.steps / dt / 1e12,
                           "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
                           "ms_per_step": dt / args.steps * 1e3, "dtype": "bf16", "config": config_of(w, "separate")}),
               flush=True)
@@ -784,6 +790,7 @@ def main():
                          "inside the consumer GEMM's epilogue; separate: coda_rms_reduce launch")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
                     help="backward: gradients of the LLaMA-8B chain from a saved forward state")
+    ap.add_argument("--compile", action="store_true", help="--impl unfused: run the unfused sequence under torch.compile")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
                     help="after warm-up run exactly one step inside cudaProfilerStart/Stop and exit (for ncu)")

@@ -126,3 +126,44 @@ def test_swiglu_save_and_backward_need_64_column_halves(lib):
     assert b"multiple of 64" in lib.coda_last_error()
     assert lib.coda_gemm_swiglu_backward(A, A + 64 * MB, A + 128 * MB, B, 256, 520, 512, 1, None) \
         == g.CODA_ERR_INVALID_ARG
+
+
+def test_gemm_layout_rules(lib):
+    # D [M, N] = A(m,k) B(n,k); operands 16-byte rows; MN-major only in bf16 and only A-with-B
+    B = A + 64 * MB
+    D = A + 128 * MB
+    ok_args = (A, 0, B, 1, D, 256, 512, 320, 1, None, None, None)
+    assert lib.coda_gemm(*ok_args[:5], 0, *ok_args[6:]) == g.CODA_OK          # M == 0: nothing to do
+    assert lib.coda_gemm(A, 1, B, 0, D, 256, 512, 320, 1, None, None, None) == g.CODA_ERR_INVALID_ARG
+    assert b"MN-major A needs" in lib.coda_last_error()
+    assert lib.coda_gemm(A, 0, B, 1, D, 256, 512, 320, 0, None, None, None) == g.CODA_ERR_INVALID_ARG  # fp32 MN
+    assert lib.coda_gemm(A, 1, B, 1, D, 100, 512, 320, 1, None, None, None) == g.CODA_ERR_INVALID_ARG  # [K, 100] rows
+    assert lib.coda_gemm(A, 0, B, 0, D, 256, 512, 300, 1, None, None, None) == g.CODA_ERR_INVALID_ARG  # K = 300
+    assert lib.coda_gemm(A, 0, B, 1, A + 4096, 256, 512, 320, 1, None, None, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_gemm(A, 2, B, 1, D, 256, 512, 320, 1, None, None, None) == g.CODA_ERR_INVALID_ARG
+
+
+def test_backward_calls_validate(lib):
+    B = A + 64 * MB
+    # grad-norm and SwiGLU backward are bf16 only
+    assert lib.coda_gemm_grad_norm(A, B, A + 128 * MB, A + 192 * MB, A + 256 * MB, A + 320 * MB, 256, 512, 512, 0,
+                                   None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_gemm_swiglu_backward(A, B, A + 128 * MB, A + 192 * MB, 256, 512, 512, 0, None) \
+        == g.CODA_ERR_INVALID_ARG
+    # RMSNorm backward: N a multiple of 8, workspace sized per 64-row chunk
+    assert lib.coda_rmsnorm_backward(A, B, A + 128 * MB, A + 129 * MB, A + 130 * MB, None, A + 192 * MB,
+                                     A + 256 * MB, A + 320 * MB, A + 321 * MB, 256, 100, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_rmsnorm_backward_workspace_bytes(256, 512) == 4 * 512 * 4
+    assert lib.coda_rmsnorm_backward_workspace_bytes(257, 512) == 5 * 512 * 4
+
+
+def test_rope_arguments_validate(lib):
+    B = A + 64 * MB
+    base = (A, B, A + 128 * MB, None, 0.0, None, A + 192 * MB, 256, 512, 512, 1, None, None)
+    # exactly one of r and P
+    assert lib.coda_gemm_rowscale_rope(A, B, None, None, 0.0, None, A + 192 * MB, 256, 512, 512, 1, None, None,
+                                       64, 256, 500000.0, 2048, None, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_gemm_rowscale_rope(*base, 60, 240, 500000.0, 2048, None, None) == g.CODA_ERR_INVALID_ARG  # head 60
+    assert lib.coda_gemm_rowscale_rope(*base, 64, 200, 500000.0, 2048, None, None) == g.CODA_ERR_INVALID_ARG  # cols
+    assert lib.coda_gemm_rowscale_rope(*base, 64, 256, 1.0, 2048, None, None) == g.CODA_ERR_INVALID_ARG      # base
+    assert lib.coda_gemm_rowscale_rope(*base, 64, 256, 500000.0, 0, None, None) == g.CODA_ERR_INVALID_ARG    # seq
