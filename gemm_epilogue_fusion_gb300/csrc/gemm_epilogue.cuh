@@ -29,7 +29,16 @@
 //   kEpiSwiGLU              act = silu(r g) * (r u): the gate and up
 //                           accumulators of the same 128 output columns share
 //                           one N=256 MMA (B tile = 128 gate rows ++ 128 up rows).
-// E4M3 operands: acc is multiplied by the per-tensor scales of A and B first.
+//   kEpiSwiGLUSave          SwiGLU that also stores the pre-activations G || U
+//                           (the "matrix block store" of the write-up's "five
+//                           blocks"), for the backward.
+//   kEpiGradNorm            backward: dY = acc stored, with the RMSNorm
+//                           backward's row sums sum_j gamma_j dY_j H_j (H loaded)
+//   kEpiSwiGLUBwd           backward: acc = dAct; dG, dU from the loaded G, U
+// The row-scale program optionally scales columns (col_scale) and applies RoPE
+// to the leading columns.  E4M3 operands: acc is multiplied by the per-tensor
+// scales of A and B first.  bf16 operands may be MN-major (stored transposed,
+// the output dimension contiguous), for the backward's transposed products.
 //
 // Two-phase launch (the whole GEMM -> RMSNorm -> GEMM block in one persistent
 // kernel): the tile sequence is every residual-GEMM tile (phase A), then every

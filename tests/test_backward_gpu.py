@@ -114,3 +114,26 @@ def test_chain_backward_llama8b_full_size_sampled_rows():
                                      W(inp["Wut"]), W(inp["Wdt"]), inp["gamma2"], W(inp["Wqt"]), w.eps, dZ[rows],
                                      dH2[rows])
     print(_check(got, ref, [p for p in CHAIN_PAIRS if p[0] in ("dX", "dR", "dh2", "dG", "dU")], rows=rows))
+
+
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_swiglu_save_matches_plain_forward_and_oracle(cg, monkeypatch):
+    """The saving forward's act equals coda_gemm_swiglu_fused_rms bit for bit,
+    and its G || U are the oracle's pre-activations (y Wg, y Wu)."""
+    import gemm_epilogue_fusion_gb300 as g
+    monkeypatch.setenv("CODA_CTA_GROUP", cg)
+    w = Workload("save", "swiglu", 300, 264, 392, 576, 0, "bf16", 1e-5, 87)
+    inp = make_inputs(w)
+    d = to_device(inp)
+    Wg = g.coda_fold_gamma(d["Wgt"], d["gamma1"])
+    Wu = g.coda_fold_gamma(d["Wut"], d["gamma1"])
+    h, P = g.coda_gemm_residual_partial_rms(d["X"], d["W1t"], d["R"])
+    act_plain = g.coda_gemm_swiglu_fused_rms(h, Wg, Wu, P, w.eps)
+    act, GU = g.coda_gemm_swiglu_save(h, Wg, Wu, P=P, eps=w.eps)
+    torch.cuda.synchronize()
+    assert torch.equal(act.cpu(), act_plain.cpu())
+    hh = oracle.gemm(inp["X"], W(inp["W1t"]), inp["R"])
+    y, _ = oracle.rmsnorm(hh, inp["gamma1"], w.eps)
+    I = w.N2
+    assert oracle.rel_err(GU[:, :I].cpu(), oracle.gemm(y, W(inp["Wgt"]))) <= TOL["bf16"]
+    assert oracle.rel_err(GU[:, I:].cpu(), oracle.gemm(y, W(inp["Wut"]))) <= TOL["bf16"]
