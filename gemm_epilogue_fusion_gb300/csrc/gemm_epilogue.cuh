@@ -186,9 +186,17 @@ __device__ __forceinline__ Tile tile_at(int t, int m_tiles, int n_tiles_a, int n
   return {1, c.m, c.n};
 }
 
-// silu(x) = x * sigmoid(x) = x / (1 + e^-x); for x -> -inf the quotient
-// goes to -0, for x -> +inf to x.
-__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+// sigmoid of two values: 1 / (1 + e^-x), with e^-x = 2^(-x log2 e) (change of
+// base) and the quotient as a reciprocal.  For x -> -inf the denominator
+// overflows and its reciprocal is 0; for x -> +inf it is 1.
+__device__ __forceinline__ float2 sigmoid2(float2 x) {
+  constexpr float kNegLog2e = -1.44269504088896341f;
+  const float2 t = fmul2(x, make_float2(kNegLog2e, kNegLog2e));
+  const float2 den = fadd2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.0f, 1.0f));
+  return make_float2(rcp_approx(den.x), rcp_approx(den.y));
+}
+// silu(x) = x * sigmoid(x), two values.
+__device__ __forceinline__ float2 silu2(float2 x) { return fmul2(x, sigmoid2(x)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
@@ -346,19 +354,48 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       const uint64_t pol_a = CODA_L2_POLICY_A, pol_b = CODA_L2_POLICY_B;
       // the stage's completion is counted on the MMA CTA's barrier
       const uint32_t full0 = C::CG == 2 ? mapa_shared(smem_u32(full), 0) : 0u;
+      // Every box of k-block kb of tile tl that this CTA loads: f(map, x, y,
+      // is_b, byte offset in the stage's A or B buffer).
+      auto boxes = [&](const Tile& tl, int kb, auto&& f) {
+        const bool pB = C::TWO_PHASE && tl.phase == 1;
+        const CUtensorMap* mA = pB ? &tmA_b : &tmA;
+        const CUtensorMap* mB = pB ? &tmB_b : &tmB;
+        [[maybe_unused]] const CUtensorMap* mB2 = pB ? &tmB2_b : &tmB2;
+        [[maybe_unused]] const bool swiglu = pB ? is_swiglu(C::kEpiB) : is_swiglu(C::kEpiA);
+        const int kx = kb * C::BK;
+        const int a_row = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
+        if constexpr (C::A_MN) {
+          // MN-major boxes: x = MN coordinate, y = k
+#pragma unroll
+          for (int i = 0; i < C::BM / C::MN_BOX; ++i) f(mA, a_row + i * C::MN_BOX, kx, false, i * C::MN_BOX_BYTES);
+        } else {
+          f(mA, kx, a_row, false, 0);
+        }
+        if constexpr (C::B_MN) {
+          const int b_row = tl.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS;
+#pragma unroll
+          for (int i = 0; i < C::B_ROWS / C::MN_BOX; ++i) f(mB, b_row + i * C::MN_BOX, kx, true, i * C::MN_BOX_BYTES);
+        } else if (swiglu) {
+          if constexpr (C::CG == 1) {  // gate rows, then up rows
+            f(mB, kx, tl.n * (C::BN / 2), true, 0);
+            f(mB2, kx, tl.n * (C::BN / 2), true, (C::BN / 2) * 128);
+          } else {  // rank 0: gate rows, rank 1: up rows
+            f(cta_rank == 0 ? mB : mB2, kx, tl.n * C::B_ROWS, true, 0);
+          }
+        } else {
+          f(mB, kx, tl.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS, true, 0);
+        }
+      };
+      auto num_kb_of = [&](const Tile& tl) {
+        return (((C::TWO_PHASE && tl.phase == 1) ? pb.K : pa.K) + C::BK - 1) / C::BK;
+      };
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
       for (int t = unit; t < num_tiles && ok; t += n_units) {
         const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
-        const bool pB = C::TWO_PHASE && tl.phase == 1;
-        const CUtensorMap* mA = pB ? &tmA_b : &tmA;
-        const CUtensorMap* mB = pB ? &tmB_b : &tmB;
-        const CUtensorMap* mB2 = pB ? &tmB2_b : &tmB2;
-        const bool swiglu = pB ? is_swiglu(C::kEpiB) : is_swiglu(C::kEpiA);
-        const int num_kb = ((pB ? pb.K : pa.K) + C::BK - 1) / C::BK;
-        const int a_row = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
-        if (pB) {
+        const int num_kb = num_kb_of(tl);
+        if (C::TWO_PHASE && tl.phase == 1) {
           // h and P of this band come from other CTAs of this launch
           if (!wait_band(&band_ready[tl.m], band_target, abort_flag)) break;
           fence_proxy_async_global();
@@ -368,49 +405,20 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             ok = false;
             break;
           }
-          const int kx = kb * C::BK;
           uint8_t* a = sA + stage * C::A_BYTES;
           uint8_t* b = sB + stage * C::B_BYTES;
-          if constexpr (C::A_MN || C::B_MN) {
-            // MN-major boxes: x = MN coordinate, y = k
-            if constexpr (C::CG == 1) mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-            else if (mma_cta) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
-            const uint32_t fb = C::CG == 2 ? full0 + static_cast<uint32_t>(stage) * 8u : 0u;
-            auto load = [&](void* dst, const CUtensorMap* m, int x, int y, uint64_t pol) {
-              if constexpr (C::CG == 1) tma_load_2d(dst, m, &full[stage], x, y, pol);
-              else tma_load_2d_pair(dst, m, fb, x, y, pol);
-            };
-            if constexpr (C::A_MN) {
-#pragma unroll
-              for (int i = 0; i < C::BM / C::MN_BOX; ++i) load(a + i * C::MN_BOX_BYTES, mA, a_row + i * C::MN_BOX, kx, pol_a);
-            } else {
-              load(a, mA, kx, a_row, pol_a);
-            }
-            const int b_row = tl.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS;
-            if constexpr (C::B_MN) {
-#pragma unroll
-              for (int i = 0; i < C::B_ROWS / C::MN_BOX; ++i) load(b + i * C::MN_BOX_BYTES, mB, b_row + i * C::MN_BOX, kx, pol_b);
-            } else {
-              load(b, mB, kx, b_row, pol_b);
-            }
-          } else if constexpr (C::CG == 1) {
+          if constexpr (C::CG == 1) {
             mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-            tma_load_2d(a, mA, &full[stage], kx, a_row, pol_a);
-            if (swiglu) {
-              tma_load_2d(b, mB, &full[stage], kx, tl.n * (C::BN / 2), pol_b);
-              tma_load_2d(b + (C::BN / 2) * 128, mB2, &full[stage], kx, tl.n * (C::BN / 2), pol_b);
-            } else {
-              tma_load_2d(b, mB, &full[stage], kx, tl.n * C::BN, pol_b);
-            }
+            boxes(tl, kb, [&](const CUtensorMap* m, int x, int y, bool is_b, int off) {
+              tma_load_2d((is_b ? b : a) + off, m, &full[stage], x, y, is_b ? pol_b : pol_a);
+            });
           } else {
             // the MMA CTA expects both CTAs' bytes; the peer only issues its copies
             if (mma_cta) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
             const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
-            tma_load_2d_pair(a, mA, fb, kx, a_row, pol_a);
-            if (swiglu)  // rank 0: gate rows, rank 1: up rows
-              tma_load_2d_pair(b, cta_rank == 0 ? mB : mB2, fb, kx, tl.n * C::B_ROWS, pol_b);
-            else
-              tma_load_2d_pair(b, mB, fb, kx, tl.n * C::BN + static_cast<int>(cta_rank) * C::B_ROWS, pol_b);
+            boxes(tl, kb, [&](const CUtensorMap* m, int x, int y, bool is_b, int off) {
+              tma_load_2d_pair((is_b ? b : a) + off, m, fb, x, y, is_b ? pol_b : pol_a);
+            });
           }
           ++issued;
           if (++stage == C::STAGES) {
@@ -612,20 +620,32 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           for (int c = 0; c < 8; ++c) {
             float o[C::CHUNK_COLS];
             float gs[EPI == kEpiSwiGLUSave ? C::CHUNK_COLS : 1], us[EPI == kEpiSwiGLUSave ? C::CHUNK_COLS : 1];
+            if constexpr (is_swiglu(EPI)) {
+              // two columns per step on the packed fp32 pipe
 #pragma unroll
-            for (int e = 0; e < C::CHUNK_COLS; ++e) {
-              const int j = c * C::CHUNK_COLS + e;
-              const float a = __uint_as_float(g[j >> 5][j & 31]);
-              if constexpr (is_swiglu(EPI)) {
-                const float uu = __uint_as_float(u[j >> 5][j & 31]);
-                const float G = a * sg, U = uu * su;
-                o[e] = silu_f(G) * U;
+              for (int e = 0; e < C::CHUNK_COLS; e += 2) {
+                const int j = c * C::CHUNK_COLS + e;
+                const float2 G = fmul2(make_float2(__uint_as_float(g[j >> 5][j & 31]),
+                                                   __uint_as_float(g[(j + 1) >> 5][(j + 1) & 31])),
+                                       make_float2(sg, sg));
+                const float2 U = fmul2(make_float2(__uint_as_float(u[j >> 5][j & 31]),
+                                                   __uint_as_float(u[(j + 1) >> 5][(j + 1) & 31])),
+                                       make_float2(su, su));
+                const float2 O = fmul2(silu2(G), U);
+                o[e] = O.x;
+                o[e + 1] = O.y;
                 if constexpr (EPI == kEpiSwiGLUSave) {
-                  gs[e] = G;
-                  us[e] = U;
+                  gs[e] = G.x;
+                  gs[e + 1] = G.y;
+                  us[e] = U.x;
+                  us[e + 1] = U.y;
                 }
-              } else {
-                o[e] = a * sg;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < C::CHUNK_COLS; ++e) {
+                const int j = c * C::CHUNK_COLS + e;
+                o[e] = __uint_as_float(g[j >> 5][j & 31]) * sg;
               }
             }
             if constexpr (EPI == kEpiSwiGLUSave) {
@@ -679,25 +699,26 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               }
               *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
             } else if constexpr (C::OUT_ELEM == 2 && EPI == kEpiSwiGLUBwd) {
-              // act = silu(G) U: dG = dAct U sigmoid(G) (1 + G (1 - sigmoid(G))), dU = dAct G sigmoid(G)
+              // act = silu(G) U: dG = dAct U silu'(G), dU = dAct silu(G)
               void* p2 = sp2 + swz(row_in_tile, c);
               const uint4 gv = *reinterpret_cast<const uint4*>(p), uv = *reinterpret_cast<const uint4*>(p2);
               const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
               uint32_t wg[4], wu[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                float dg[2], du[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const float G = h ? bf16_hi(gw[e]) : bf16_lo(gw[e]);
-                  const float U = h ? bf16_hi(uw[e]) : bf16_lo(uw[e]);
-                  const float sgm = __fdividef(1.0f, 1.0f + __expf(-G));
-                  const float da = o[2 * e + h];
-                  dg[h] = da * U * sgm * (1.0f + G * (1.0f - sgm));
-                  du[h] = da * G * sgm;
-                }
-                wg[e] = pack_bf16x2(dg[0], dg[1]);
-                wu[e] = pack_bf16x2(du[0], du[1]);
+                // two columns at a time: s = sigmoid(G), silu(G) = G s,
+                // silu'(G) = s (1 + G (1 - s)) = s + silu(G) (1 - s)
+                const float2 G = make_float2(bf16_lo(gw[e]), bf16_hi(gw[e]));
+                const float2 U = make_float2(bf16_lo(uw[e]), bf16_hi(uw[e]));
+                const float2 da = make_float2(o[2 * e], o[2 * e + 1]);
+                const float2 s = sigmoid2(G);
+                const float2 gs = fmul2(G, s);
+                const float2 one_minus_s = ffma2(s, make_float2(-1.0f, -1.0f), make_float2(1.0f, 1.0f));
+                const float2 dsilu = ffma2(gs, one_minus_s, s);
+                const float2 dg = fmul2(fmul2(da, U), dsilu);
+                const float2 du = fmul2(da, gs);
+                wg[e] = pack_bf16x2(dg.x, dg.y);
+                wu[e] = pack_bf16x2(du.x, du.y);
               }
               *reinterpret_cast<uint4*>(p) = make_uint4(wg[0], wg[1], wg[2], wg[3]);
               *reinterpret_cast<uint4*>(p2) = make_uint4(wu[0], wu[1], wu[2], wu[3]);
