@@ -760,7 +760,7 @@ def run_unfused(args, w):
         step()
     torch.cuda.synchronize()
     if args.profile_step:
-        profile_one_step(step, rank, "unfused torch eager", None)
+        profile_one_step(step, rank, "unfused torch.compile" if args.compile else "unfused torch eager", None)
         return
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
@@ -777,6 +777,79 @@ def run_unfused(args, w):
               flush=True)
 
 
+def run_aux(args, w):
+    """The HBM-bound kernels of the path at this workload's sizes: GB/s and the
+    fraction of the measured HBM copy bandwidth.  Bytes are algorithmic (every
+    operand read and every output written once); 3 rotating input sets, each
+    larger than L2 where the operands are (P and r are tiny and stay in L2)."""
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import gemm_epilogue_fusion_gb300 as g
+    g.load_library()
+    M, N = w.M, w.N
+    I = w.inter or w.N2
+    T = g.coda_partial_cols(N)
+    gen = torch.Generator(device=dev).manual_seed(11)
+    bf = torch.bfloat16
+
+    def rnd(*s, dt=bf):
+        return torch.randn(*s, generator=gen, device=dev).to(dt)
+
+    sets = []
+    for _ in range(NSETS):
+        sets.append({"W": rnd(I, N), "gam": rnd(N, dt=torch.float32).abs() + 0.5, "Wo": torch.empty(I, N, dtype=bf, device=dev),
+                     "P": rnd(M, T, dt=torch.float32).abs() * N / T, "r": torch.empty(M, device=dev),
+                     "H": rnd(M, N), "dY": rnd(M, N), "S": rnd(M, T, dt=torch.float32),
+                     "dH": torch.empty(M, N, dtype=bf, device=dev), "Yt": torch.empty(M, N, dtype=bf, device=dev),
+                     "dgam": torch.empty(N, device=dev), "amax": torch.empty(1, device=dev),
+                     "q": torch.empty(M, N, dtype=torch.uint8, device=dev), "scale": torch.empty(1, device=dev)})
+    ws_bytes = g.load_library().coda_rmsnorm_backward_workspace_bytes(M, N)
+    wsp = torch.empty(max(ws_bytes // 4, 1), dtype=torch.float32, device=dev)
+    for s in sets:
+        s["rr"] = torch.rand(M, device=dev) + 0.5
+    kernels = {
+        "fold_gamma": (lambda s: g.coda_fold_gamma(s["W"], s["gam"], out=s["Wo"]), 2 * I * N * 2 + 4 * N,
+                       f"W^T [{I}x{N}] bf16 -> diag(gamma)-folded copy"),
+        "rms_reduce": (lambda s: g.coda_rms_reduce(s["P"], N, w.eps, r=s["r"]), 4 * M * T + 4 * M,
+                       f"P [{M}x{T}] fp32 -> r [{M}] (L2-resident, latency-bound)"),
+        "amax": (lambda s: g.coda_amax(s["H"], amax=s["amax"]), 2 * M * N, f"max |h| over [{M}x{N}] bf16"),
+        "quantize_e4m3": (lambda s: g.coda_quantize_e4m3(s["H"], s["amax"], q=s["q"], scale=s["scale"]), 3 * M * N,
+                          f"h [{M}x{N}] bf16 -> e4m3"),
+        "rmsnorm_backward": (lambda s: g.coda_rmsnorm_backward(s["dY"], s["H"], s["rr"], s["gam"], s["S"], dH=s["dH"],
+                                                                Yt=s["Yt"], dgamma=s["dgam"], workspace=wsp),
+                             4 * M * N * 2 + 4 * M * T + 4 * M + 8 * N,
+                             f"dY, h [{M}x{N}] bf16 -> dh, r h bf16, dgamma"),
+    }
+    for s in sets:  # amax before quantise
+        g.coda_amax(s["H"], amax=s["amax"])
+    pk, pk_kind = peaks()
+    out = {}
+    clk = ClockSampler(local)
+    with clk:
+        for name, (fn, nbytes, what) in kernels.items():
+            for i in range(args.warmup):
+                fn(sets[i % NSETS])
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = max(args.steps, 10)
+            a.record()
+            for i in range(n):
+                fn(sets[i % NSETS])
+            b.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / n
+            gbs = nbytes / (us * 1e-6) / 1e9
+            out[name] = {"us_per_launch": us, "bytes_per_launch": nbytes, "GB/s": gbs, "frac": gbs / pk["hbm_gbs"],
+                         "what": what}
+    if g.coda_get_device_status() != 0:
+        raise SystemExit("device status not clean")
+    print(json.dumps({"pass": "aux", "metric": "HBM GB/s of the memory-bound kernels", "unit": "GB/s",
+                      "peak": pk["hbm_gbs"], "peak_kind": f"HBM copy, {pk_kind}", "kernels": out,
+                      "steps": n, "config": {"workload": w.name, "M": M, "N": N, "I": I, "T": T},
+                      "clocks": clk.summary()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -790,8 +863,9 @@ def main():
     ap.add_argument("--reduce", choices=["block", "fused", "separate"], default="block",
                     help="block: residual GEMM and consumer in one persistent launch per block; fused: r reduced "
                          "inside the consumer GEMM's epilogue; separate: coda_rms_reduce launch")
-    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
-                    help="backward: gradients of the LLaMA-8B chain from a saved forward state")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "aux"], default="forward",
+                    help="backward: gradients of the LLaMA-8B chain from a saved forward state; aux: GB/s of the "
+                         "memory-bound kernels (fold, reduce, amax, quantise, RMSNorm backward)")
     ap.add_argument("--compile", action="store_true", help="--impl unfused: run the unfused sequence under torch.compile")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
@@ -803,7 +877,11 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
-    if args.pass_ == "backward":
+    if args.pass_ == "aux":
+        if args.impl != "coda":
+            ap.error("--pass aux measures this library's kernels only")
+        run_aux(args, w)
+    elif args.pass_ == "backward":
         if w.chain != "full" or w.dtype != "bf16":
             ap.error("--pass backward covers the bf16 LLaMA-8B chain (--workload llama8b_chain)")
         if args.impl == "unfused":
