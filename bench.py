@@ -653,6 +653,9 @@ def run_coda_backward(args, w):
     for i in range(args.warmup):
         step(sets[i % 2])
     g.coda_get_device_status()
+    if args.profile_step:
+        profile_one_step(lambda: step(sets[0]), rank, "coda backward", 12)
+        return
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -823,6 +826,13 @@ def run_aux(args, w):
     }
     for s in sets:  # amax before quantise
         g.coda_amax(s["H"], amax=s["amax"])
+    if args.profile_step:
+        for i in range(args.warmup):
+            for fn, _, _ in kernels.values():
+                fn(sets[i % NSETS])
+        profile_one_step(lambda: [fn(sets[0]) for fn, _, _ in kernels.values()], 0, "coda aux kernels",
+                         len(kernels) + 1)
+        return
     pk, pk_kind = peaks()
     out = {}
     clk = ClockSampler(local)
@@ -870,6 +880,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
                     help="after warm-up run exactly one step inside cudaProfilerStart/Stop and exit (for ncu)")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="with --profile-step: override the workload's M (tokens), for ncu captures on a smaller "
+                         "case of the same kernels")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for warm-up + timed steps together")
@@ -877,6 +890,10 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
+    if args.rows:
+        if not args.profile_step:
+            ap.error("--rows is for --profile-step captures only")
+        w = w.with_rows(args.rows)
     if args.pass_ == "aux":
         if args.impl != "coda":
             ap.error("--pass aux measures this library's kernels only")
