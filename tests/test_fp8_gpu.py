@@ -51,6 +51,31 @@ def test_amax_and_quantize_codes_bit_exact(dtype):
     assert np.all((got[zero] & 0x7F) == 0)
 
 
+@pytest.mark.parametrize("scale_exp", [0, -60, 60, -110])
+def test_quantize_codes_equal_correctly_rounded_quotient_at_scale(scale_exp):
+    """Four million values over 12 binades, with the whole tensor shifted by
+    2^scale_exp so that s covers the FMA-division path and (at 2^-110) the
+    plain-divide fallback.  The reference quotient is x / s in float64 rounded
+    to float32: 53 >= 2 * 24 + 2 bits, so that double rounding equals the
+    correctly rounded float32 quotient.  Its e4m3 code is torch's RNE cast."""
+    import gemm_epilogue_fusion_gb300 as g
+    gen = torch.Generator(device="cuda").manual_seed(77 + scale_exp)
+    n = (1 << 22) + 5
+    e = torch.randint(-12, 1, (n,), generator=gen, device="cuda").float() + scale_exp
+    x = torch.randn(n, generator=gen, device="cuda") * torch.exp2(e)
+    amax = g.coda_amax(x)
+    q, s = g.coda_quantize_e4m3(x, amax)
+    torch.cuda.synchronize()
+    s64 = torch.tensor(np.float32(x.abs().max().item()) / np.float32(448.0), dtype=torch.float64, device="cuda")
+    assert float(s.item()) == float(s64.item())
+    quot = (x.double() / s64).float()
+    want = quot.to(torch.float8_e4m3fn).view(torch.uint8)
+    got = q
+    zero = (want & 0x7F) == 0
+    assert torch.equal(got[~zero], want[~zero])
+    assert bool(torch.all((got[zero] & 0x7F) == 0))
+
+
 def test_quantize_all_zero_uses_unit_scale():
     import gemm_epilogue_fusion_gb300 as g
     d = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
