@@ -75,10 +75,19 @@ def algorithmic_bytes(M, K1, N, I, T):
     return fused, unfused
 
 
-def kernel_source_sha():
+# Sources each kernel family is compiled from: a recorded ncu figure is valid
+# while the hash of its family's files is unchanged.
+KERNEL_SOURCES = {
+    "gemm": ["coda_internal.h", "gemm_epilogue.cuh", "sm103_ptx.cuh", "coda_gemm_bf16.cu", "coda_gemm_tf32.cu",
+             "coda_gemm_e4m3.cu"],
+    "aux": ["coda_internal.h", "sm103_ptx.cuh", "coda_aux.cu"],
+}
+
+
+def kernel_source_sha(family="gemm"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_epilogue_fusion_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(KERNEL_SOURCES[family]):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
