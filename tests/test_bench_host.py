@@ -30,13 +30,18 @@ def test_fused_moves_fewer_bytes_than_unfused():
 
 def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", {"gemm": ["k.cu", "k.cuh"], "aux": ["a.cu"]})
     csrc = tmp_path / "gemm_epilogue_fusion_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (csrc / "k.cu").write_text("kernel v1")
+    (csrc / "k.cuh").write_text("header v1")
+    (csrc / "a.cu").write_text("aux v1")
     (tmp_path / "profiles").mkdir()
     sha = bench.kernel_source_sha()
     (tmp_path / "profiles" / "ncu_x.md").write_text(f"source_sha: {sha}\ndram_bytes_per_launch: 1.5e8\n")
     assert bench.recorded_traffic("x") == 1.5e8
-    (csrc / "k.cu").write_text("kernel v2")
+    (csrc / "a.cu").write_text("aux v2")  # another kernel family: the GEMM figure stays valid
+    assert bench.recorded_traffic("x") == 1.5e8
+    (csrc / "k.cuh").write_text("header v2")
     assert bench.recorded_traffic("x") is None
     assert bench.recorded_traffic("missing") is None
