@@ -332,11 +332,13 @@ CODA_API coda_status coda_gemm_swiglu_backward(const void* dOut, const void* Wt,
 CODA_API coda_status coda_amax(const void* x, int64_t n, coda_dtype dtype, float* amax, cudaStream_t stream);
 
 /* Per-tensor FP8 quantisation with the scale s = amax / 448 (s = 1 when
- * amax == 0): q_i = e4m3(x_i / s), rounded to nearest-even and saturated to
- * +-448 (OCP e4m3, no infinities).  x [n] CODA_F32 or CODA_BF16; amax: device
- * fp32 scalar from coda_amax or from a GEMM's amax output; q [n] bytes
- * (16-byte aligned, n a multiple of 16); scale: device fp32 scalar receiving s,
- * the dequantisation scale to pass to the GEMMs. */
+ * amax == 0): q_i = e4m3(x_i / s), where x_i / s is the correctly rounded fp32
+ * quotient, then rounded to nearest-even and saturated to +-448 (OCP e4m3, no
+ * infinities).  x [n] CODA_F32 or CODA_BF16; amax: device fp32 scalar from
+ * coda_amax or from a GEMM's amax output; q [n] bytes; x and q 16-byte
+ * aligned, any n >= 0 (a tail of n mod 16 elements takes a scalar path);
+ * scale: device fp32 scalar receiving s, the dequantisation scale to pass to
+ * the GEMMs.  q and scale may not overlap x or amax. */
 CODA_API coda_status coda_quantize_e4m3(const void* x, int64_t n, coda_dtype dtype, const float* amax, uint8_t* q,
                                float* scale, cudaStream_t stream);
 
