@@ -1,8 +1,9 @@
 /*
  * coda.h -- C ABI of the GB300 (sm_103a) fused GEMM-epilogue library.
  *
- * The library implements the forward hot path of "CODA: Rewriting Transformer
- * Blocks as GEMM-Epilogue Programs" as the CODA news write-up describes it
+ * The library implements the hot path of "CODA: Rewriting Transformer Blocks
+ * as GEMM-Epilogue Programs", forward and backward, as the CODA news write-up
+ * describes it
  * (KuCoin news, "CODA new research optimizes transformer training with
  * GEMM-epilogue programming"; the same article on itsolotime.com and on
  * KuCoin's Arabic site):
@@ -26,6 +27,12 @@
  *     Z    = diag(r) . h . W2'      == RMSNorm(h).W2   coda_gemm_rowscale
  *     act  = silu(r h Wg') * (r h Wu')                 coda_gemm_swiglu
  * with RMSNorm(h)_ij = h_ij * r_i * gamma_j and silu(x) = x / (1 + e^-x).
+ * Further calls fold r into the consumer GEMM (coda_gemm_*_fused_rms), run a
+ * residual GEMM and its consumer as one launch (coda_block_*), rotate Q and K
+ * in the QKV GEMM's epilogue (coda_gemm_rowscale_rope), give the backward of
+ * the block (coda_gemm_grad_norm, coda_rmsnorm_backward, coda_gemm with
+ * either operand layout, coda_gemm_swiglu_save / coda_gemm_swiglu_backward),
+ * and quantise to FP8 (coda_amax, coda_quantize_e4m3).
  *
  * Conventions shared by every call
  *   - Matrices are row-major.  Activations are [rows, K]; a weight W [K, N]
