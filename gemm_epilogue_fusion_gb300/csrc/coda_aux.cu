@@ -232,10 +232,10 @@ __global__ void __launch_bounds__(kBwdThreads) rmsnorm_bwd_kernel(
   }
   const int nv = N / 8;
   const int rows = min(kBwdRows, M - row0);
-  for (int ii = 0; ii < rows; ++ii) {
-    const int64_t v = static_cast<int64_t>(row0 + ii) * nv + col / 8;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  // one row of this thread's 8 columns: stores dh and r h, accumulates dgamma
+  auto row_out = [&](int ii, int64_t v, const uint4& a, const uint4& b, const uint4& d) {
     const float ri = s_r[ii], ci = s_c[ii];
-    uint4 a = __ldg(dY + v), b = __ldg(H + v), d = dH_in ? __ldg(dH_in + v) : make_uint4(0, 0, 0, 0);
     const __nv_bfloat162* ya = reinterpret_cast<const __nv_bfloat162*>(&a);
     const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&b);
     const __nv_bfloat162* dd = reinterpret_cast<const __nv_bfloat162*>(&d);
@@ -252,20 +252,54 @@ __global__ void __launch_bounds__(kBwdThreads) rmsnorm_bwd_kernel(
     }
     dH[v] = o1;
     Yt[v] = o2;
+  };
+  // rows in groups of 4: all loads of a group are issued before any use, so
+  // a thread keeps 8-12 16-byte loads in flight; rows are still consumed in
+  // order, so dgamma's partial sums are unchanged
+  int ii = 0;
+  for (; ii + 4 <= rows; ii += 4) {
+    uint4 a[4], b[4], d[4];
+    int64_t v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      v[u] = static_cast<int64_t>(row0 + ii + u) * nv + col / 8;
+      a[u] = __ldg(dY + v[u]);
+      b[u] = __ldg(H + v[u]);
+      d[u] = dH_in ? __ldg(dH_in + v[u]) : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) row_out(ii + u, v[u], a[u], b[u], d[u]);
+  }
+  for (; ii < rows; ++ii) {
+    const int64_t v = static_cast<int64_t>(row0 + ii) * nv + col / 8;
+    row_out(ii, v, __ldg(dY + v), __ldg(H + v), dH_in ? __ldg(dH_in + v) : zero);
   }
   float4* pp = reinterpret_cast<float4*>(part + static_cast<int64_t>(blockIdx.y) * N + col);
   pp[0] = make_float4(dg[0], dg[1], dg[2], dg[3]);
   pp[1] = make_float4(dg[4], dg[5], dg[6], dg[7]);
 }
 
-// dgamma[j] = sum over chunks of part[chunk, j], in chunk order.
-__global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict__ part, int chunks, int N,
-                                                         float* __restrict__ out) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= N) return;
-  float s = 0.0f;
-  for (int c = 0; c < chunks; ++c) s += part[static_cast<int64_t>(c) * N + j];
-  out[j] = s;
+// dgamma[j] = sum over chunks of part[chunk, j]: the 8 warps of a block each
+// sum every 8th chunk in chunk order for 32 columns, then warp 0 adds the 8
+// partial sums in warp order.  The order is fixed, so the result is the same
+// on every run.
+constexpr int kColSumWarps = 8;
+__global__ void __launch_bounds__(32 * kColSumWarps) column_sum_kernel(const float* __restrict__ part, int chunks,
+                                                                       int N, float* __restrict__ out) {
+  __shared__ float s[kColSumWarps][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int j = blockIdx.x * 32 + lane;
+  float acc = 0.0f;
+  if (j < N)
+    for (int c = w; c < chunks; c += kColSumWarps) acc += part[static_cast<int64_t>(c) * N + j];
+  s[w][lane] = acc;
+  __syncthreads();
+  if (w == 0 && j < N) {
+    float sum = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kColSumWarps; ++k) sum += s[k][lane];
+    out[j] = sum;
+  }
 }
 
 int grid_for(int64_t work_items, int threads) {
@@ -311,7 +345,8 @@ cudaError_t launch_rmsnorm_backward(const void* dY, const void* H, const float* 
       static_cast<uint4*>(dH), static_cast<uint4*>(Yt), part, static_cast<int>(M), static_cast<int>(N));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  column_sum_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(part, chunks, static_cast<int>(N), dgamma);
+  column_sum_kernel<<<static_cast<unsigned>((N + 31) / 32), 32 * kColSumWarps, 0, s>>>(part, chunks, static_cast<int>(N),
+                                                                                dgamma);
   return cudaGetLastError();
 }
 
