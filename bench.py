@@ -84,12 +84,20 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace runs collapsed, so an
+    edit of the comments leaves the hash of the compiled code unchanged."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha(family="gemm"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_epilogue_fusion_gb300", "csrc")
     for f in sorted(KERNEL_SOURCES[family]):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,8 +1,9 @@
 // Persistent, warp-specialised tcgen05 GEMM with fused epilogue programs.
 //
-// D[M, N_out] = epilogue(A[M, K] . B[N_out, K]^T), both operands K-major
-// (activations [M, K] and weights W^T [N_out, K], row-major), TMA-loaded with
-// 128-byte swizzle so every k-block row of a tile is exactly 128 bytes.
+// D[M, N_out] = epilogue(A[M, K] . B[N_out, K]^T), operands K-major by default
+// (activations [M, K] and weights W^T [N_out, K], row-major; MN-major for the
+// backward's transposed products, see below), TMA-loaded with 128-byte swizzle
+// so every k-block row of a tile is exactly 128 bytes.
 //
 // One CTA (or one cluster pair of CTAs, tcgen05 cta_group::2) per SM walks
 // output tiles of 128 (256) rows.  Roles (warps):
@@ -13,10 +14,11 @@
 //   2..5   epilogue: tcgen05.ld (one accumulator row per thread) -> fused
 //          program -> 128B-swizzled shared slot -> TMA store, one 128-byte
 //          wide column box at a time
-//   6      residual program: TMA loads of R boxes into the slot ring, so the
-//          residual add reads R from shared memory and writes h in place; in
-//          a two-phase launch it also hands the slots of the second phase's
-//          boxes to the epilogue
+//   6      programs that read a tile of another tensor (R of the residual,
+//          H of the grad-norm, G and U of the SwiGLU backward): TMA loads of
+//          those boxes into the slot ring, so the epilogue reads them from
+//          shared memory and writes its result in place; in a two-phase launch
+//          it also hands the slots of the second phase's boxes to the epilogue
 //
 // Epilogue programs.  The CODA write-ups ("CODA: the treasure hidden in the
 // epilogue") apply the memory-bound neighbours of a GEMM while its product is
@@ -28,7 +30,8 @@
 //                           the second GEMM (gamma is folded into its weight).
 //   kEpiSwiGLU              act = silu(r g) * (r u): the gate and up
 //                           accumulators of the same 128 output columns share
-//                           one N=256 MMA (B tile = 128 gate rows ++ 128 up rows).
+//                           one N=256 MMA (B tile = 128 gate rows ++ 128 up rows);
+//                           two columns per instruction on the packed f32x2 pipe.
 //   kEpiSwiGLUSave          SwiGLU that also stores the pre-activations G || U
 //                           (the "matrix block store" of the write-up's "five
 //                           blocks"), for the backward.

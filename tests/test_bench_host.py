@@ -42,6 +42,8 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("x") == 1.5e8
     (csrc / "a.cu").write_text("aux v2")  # another kernel family: the GEMM figure stays valid
     assert bench.recorded_traffic("x") == 1.5e8
+    (csrc / "k.cu").write_text("kernel   v1 // a comment\n/* and a\n block */")  # comments and spacing only
+    assert bench.recorded_traffic("x") == 1.5e8
     (csrc / "k.cuh").write_text("header v2")
     assert bench.recorded_traffic("x") is None
     assert bench.recorded_traffic("missing") is None
