@@ -69,6 +69,7 @@ SIGNATURES = {
     "coda_gemm_swiglu_save": (_i32, [_vp, _vp, _vp, _fp, _fp, _f32, _fp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
     "coda_amax": (_i32, [_vp, _i64, _i32, _fp, _vp]),
     "coda_quantize_e4m3": (_i32, [_vp, _i64, _i32, _fp, _vp, _fp, _vp]),
+    "coda_selftest_wait_timeout": (_i32, [_i64, _vp]),
     "coda_get_device_status": (_i32, []),
 }
 
@@ -418,6 +419,17 @@ def coda_quantize_e4m3(x, amax, q=None, scale=None, stream=None):
     _check(lib.coda_quantize_e4m3(_dev(x, "x"), x.numel(), _dtype_code(x), _dev(amax, "amax"), _dev(q, "q"),
                                   _dev(scale, "scale"), _stream(x, stream)))
     return q, scale
+
+
+def coda_selftest_wait_timeout(timeout_ns: int, stream=None):
+    """Enqueue the failure-path self-test: a bounded wait on an mbarrier that
+    nothing signals gives up after timeout_ns and raises the timeout bit, so
+    the next coda_get_device_status() raises CodaError(CODA_ERR_TIMEOUT)."""
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(lib.coda_selftest_wait_timeout(int(timeout_ns), s))
 
 
 def coda_get_device_status() -> int:

@@ -814,6 +814,14 @@ coda_status coda_quantize_e4m3(const void* x, int64_t n, coda_dtype dtype, const
   return e == cudaSuccess ? CODA_OK : cuda_fail(e, "coda_quantize_e4m3 launch");
 }
 
+coda_status coda_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE(timeout_ns >= 1000 && timeout_ns <= 10000000000LL,
+          "coda_selftest_wait_timeout: timeout_ns must lie in [1e3, 1e10]");
+  cudaError_t e = coda::launch_wait_probe(timeout_ns, stream);
+  return e == cudaSuccess ? CODA_OK : cuda_fail(e, "coda_selftest_wait_timeout launch");
+}
+
 coda_status coda_get_device_status(void) {
   g_msg[0] = 0;
   cudaError_t e = cudaDeviceSynchronize();

@@ -302,6 +302,27 @@ __global__ void __launch_bounds__(32 * kColSumWarps) column_sum_kernel(const flo
   }
 }
 
+// Status word of this translation unit, read back (and cleared) by
+// read_clear_status_aux(): the wait probe's timeout bit.
+__device__ unsigned g_aux_status;
+
+// Self-test of the failure path: one thread waits on an mbarrier that nothing
+// signals, bounded by timeout_ns of %globaltimer like every wait of the GEMM
+// kernels, then raises the timeout bit and returns, leaving the context usable.
+__global__ void __launch_bounds__(32) wait_probe_kernel(uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  const uint32_t a = smem_u32(&bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, 0u)) {  // phase 0 of a fresh barrier never completes
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      atomicOr(&g_aux_status, kDevTimeout);
+      return;
+    }
+  }
+}
+
 int grid_for(int64_t work_items, int threads) {
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
   int64_t g = (work_items + threads - 1) / threads;
@@ -369,6 +390,16 @@ cudaError_t launch_quantize_e4m3(const void* x, int64_t n, bool f32, const float
   return cudaGetLastError();
 }
 
-unsigned read_clear_status_aux() { return 0u; }
+cudaError_t launch_wait_probe(int64_t timeout_ns, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(static_cast<uint64_t>(timeout_ns));
+  return cudaGetLastError();
+}
+
+unsigned read_clear_status_aux() {
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_aux_status, sizeof(v)) != cudaSuccess) return ~0u;
+  if (cudaMemcpyToSymbol(g_aux_status, &zero, sizeof(zero)) != cudaSuccess) return ~0u;
+  return v;
+}
 
 }  // namespace coda

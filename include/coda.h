@@ -349,6 +349,16 @@ CODA_API coda_status coda_amax(const void* x, int64_t n, coda_dtype dtype, float
 CODA_API coda_status coda_quantize_e4m3(const void* x, int64_t n, coda_dtype dtype, const float* amax, uint8_t* q,
                                float* scale, cudaStream_t stream);
 
+/* Self-test of the failure path, with no GPU fault: enqueues one block whose
+ * thread waits on a shared-memory mbarrier that nothing signals.  The wait is
+ * bounded by timeout_ns of the GPU's global timer, like every wait inside the
+ * GEMM kernels (which use 2 s).  When the limit runs out the thread raises
+ * the timeout bit of the device status word and the kernel returns, so the
+ * next coda_get_device_status() reports CODA_ERR_TIMEOUT and the context
+ * stays usable.  Not on the pages: a diagnostic of this library.
+ *   timeout_ns in [1e3, 1e10] (else CODA_ERR_INVALID_ARG, nothing enqueued). */
+CODA_API coda_status coda_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream);
+
 /* Synchronises the current device, then reads and clears the device status
  * word: CODA_ERR_TIMEOUT if any kernel since the last call gave up on a
  * bounded wait, CODA_ERR_CUDA if the device reports an error, else CODA_OK. */

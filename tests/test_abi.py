@@ -167,3 +167,11 @@ def test_rope_arguments_validate(lib):
     assert lib.coda_gemm_rowscale_rope(*base, 64, 200, 500000.0, 2048, None, None) == g.CODA_ERR_INVALID_ARG  # cols
     assert lib.coda_gemm_rowscale_rope(*base, 64, 256, 1.0, 2048, None, None) == g.CODA_ERR_INVALID_ARG      # base
     assert lib.coda_gemm_rowscale_rope(*base, 64, 256, 500000.0, 0, None, None) == g.CODA_ERR_INVALID_ARG    # seq
+
+
+def test_selftest_timeout_range(lib):
+    # the failure-path self-test only takes a bounded, sensible limit
+    assert lib.coda_selftest_wait_timeout(0, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_selftest_wait_timeout(999, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_selftest_wait_timeout(10_000_000_001, None) == g.CODA_ERR_INVALID_ARG
+    assert b"timeout_ns" in lib.coda_last_error()
