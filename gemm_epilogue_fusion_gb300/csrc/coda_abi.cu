@@ -16,6 +16,11 @@
 #include "coda.h"
 #include "coda_internal.h"
 
+namespace coda {
+// The failure-path self-test kernel's launcher (coda_aux.cu).
+cudaError_t launch_wait_probe(int64_t timeout_ns, cudaStream_t s);
+}  // namespace coda
+
 namespace {
 
 thread_local char g_msg[512] = "";

@@ -122,7 +122,6 @@ cudaError_t launch_rmsnorm_backward(const void* dY, const void* H, const float* 
 cudaError_t launch_amax(const void* x, int64_t n, bool f32, float* amax, cudaStream_t s);
 cudaError_t launch_quantize_e4m3(const void* x, int64_t n, bool f32, const float* amax, uint8_t* q,
                                  float* scale, cudaStream_t s);
-cudaError_t launch_wait_probe(int64_t timeout_ns, cudaStream_t s);
 unsigned read_clear_status_aux();
 
 // Host helpers (coda_abi.cu).
