@@ -189,6 +189,37 @@ __device__ __forceinline__ Tile tile_at(int t, int m_tiles, int n_tiles_a, int n
   return {1, c.m, c.n};
 }
 
+// The k-th tile index of unit u (a CTA or a CTA pair) out of U units, or a
+// value >= n_a + n_b once u has no tiles left.  Phase-A tiles are dealt round
+// robin, so the first r_a = n_a mod U units hold one more of them.  A phase-A
+// tile costs about `d` phase-B tiles (the ratio of their k-blocks), so those
+// units sit out the first d rounds of phase B, which go round robin to the
+// other units; the rest of phase B is dealt round robin to every unit.  Each
+// unit then ends with about the same number of k-blocks, and consecutive
+// indices still run side by side (the raster's L2 reuse).  Every unit walks
+// all its phase-A tiles before any phase-B tile.  One-phase launches (n_b = 0)
+// get the plain round robin u, u + U, u + 2U, ...
+__host__ __device__ inline int walk_tile(int u, int k, int U, int n_a, int n_b, int d) {
+  const int q_a = n_a / U, r_a = n_a % U;
+  const int others = U - r_a;
+  // plain round robin when phase A divides evenly, when a phase-A tile costs
+  // about one phase-B tile (the round robin then already hands the first
+  // phase-B round to the units without the extra phase-A tile), or when there
+  // is not one whole phase-B round
+  if (r_a == 0 || d <= 1 || n_b < others) return u + k * U;
+  const int own_a = q_a + (u < r_a ? 1 : 0);
+  if (k < own_a) return u + k * U;
+  int kb = k - own_a;
+  const int rounds = min(d, n_b / others);  // whole head rounds only
+  const int head = rounds * others;
+  if (u >= r_a) {
+    if (kb < rounds) return n_a + (u - r_a) + kb * others;
+    kb -= rounds;
+  }
+  const int j = head + u + kb * U;
+  return n_a + (j < n_b ? j : n_b);
+}
+
 // sigmoid of two values: 1 / (1 + e^-x), with e^-x = 2^(-x log2 e) (change of
 // base) and the quotient as a reciprocal.  For x -> -inf the denominator
 // overflows and its reciprocal is 0; for x -> +inf it is 1.
@@ -301,6 +332,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   const int n_tiles_a = (pa.N_out + C::out_cols(C::kEpiA) - 1) / C::out_cols(C::kEpiA);
   const int n_tiles_b = C::TWO_PHASE ? (pb.N_out + C::out_cols(C::kEpiB) - 1) / C::out_cols(C::kEpiB) : 0;
   const int num_tiles = m_tiles * (n_tiles_a + n_tiles_b);
+  // phase-B rounds that units holding an extra phase-A tile sit out
+  const int b_rounds = C::TWO_PHASE ? ((pa.K + C::BK - 1) / C::BK + ((pb.K + C::BK - 1) / C::BK) / 2) /
+                                          max(1, (pb.K + C::BK - 1) / C::BK)
+                                    : 0;
+  auto walk = [&](int k) { return walk_tile(unit, k, n_units, m_tiles * n_tiles_a, m_tiles * n_tiles_b, b_rounds); };
   // a band is ready for phase B when every phase-A tile of it (one increment
   // per CTA) has stored h and P
   const unsigned band_target = static_cast<unsigned>(n_tiles_a * C::CG);
@@ -395,7 +431,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
-      for (int t = unit; t < num_tiles && ok; t += n_units) {
+      for (int k = 0; ok; ++k) {
+        const int t = walk(k);
+        if (t >= num_tiles) break;
         const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
         const int num_kb = num_kb_of(tl);
         if (C::TWO_PHASE && tl.phase == 1) {
@@ -442,7 +480,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = unit; t < num_tiles && ok; t += n_units, ++it) {
+      for (int k = 0; ok; ++k, ++it) {
+        const int t = walk(k);
+        if (t >= num_tiles) break;
         const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
         const int num_kb = (((C::TWO_PHASE && tl.phase == 1) ? pb.K : pa.K) + C::BK - 1) / C::BK;
         const int buf = it & 1;
@@ -489,7 +529,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         int slot = 0;
         uint32_t phase = 0, used = 0;
         bool ok = true;
-        for (int t = unit; t < num_tiles && ok; t += n_units) {
+        for (int k = 0; ok; ++k) {
+          const int t = walk(k);
+          if (t >= num_tiles) break;
           const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
           const bool pB = C::TWO_PHASE && tl.phase == 1;
           const int row0 = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
@@ -805,7 +847,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       }
     };
 
-    for (int t = unit; t < num_tiles && ok; t += n_units, ++it) {
+    for (int k = 0; ok; ++k, ++it) {
+      const int t = walk(k);
+      if (t >= num_tiles) break;
       const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
