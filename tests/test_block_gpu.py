@@ -80,6 +80,31 @@ def test_block_full_size_equals_separate_calls(name):
     assert torch.count_nonzero(ws).item() == 0
 
 
+def test_block_full_size_8b_chain_equals_separate_calls():
+    """The LLaMA-8B block-tail chain as two one-launch blocks (Wo + gate/up,
+    then down + QKV, the bench's default step), at full size.  The second block
+    has phase-A tiles of K = 14336 against phase-B tiles of K = 4096 and 1024
+    phase-A tiles over 76 CTA pairs, so its units walk the balanced order."""
+    import gemm_epilogue_fusion_gb300 as g
+    from gemm_epilogue_fusion_gb300 import chain as C
+    w = WORKLOADS["llama8b_chain"]
+    inp = make_inputs(w)
+    d = to_device(inp)
+    sep = run_gpu(w, d, fused_reduce=True)
+    gam = {k: d[k] for k in d if k.startswith("gamma")}
+    f = C.fold_weights("full", {k: d[k] for k in d if k.startswith("W")}, gam)
+    ws1, ws2 = g.block_workspace(w.M, "cuda"), g.block_workspace(w.M, "cuda")
+    r1 = torch.empty(w.M, dtype=torch.float32, device="cuda")
+    r2 = torch.empty(w.M, dtype=torch.float32, device="cuda")
+    h1, P1, act = g.coda_block_swiglu(d["X"], d["W1t"], d["R"], f["Wgt"], f["Wut"], w.eps, ws1, r_out=r1)
+    h2, P2, Z = g.coda_block_rowscale(act, d["Wdt"], h1, f["Wqt"], w.eps, ws2, r_out=r2)
+    torch.cuda.synchronize()
+    blk = {"h1": h1, "r1": r1, "act": act, "h2": h2, "r2": r2, "Z": Z}
+    for k, v in blk.items():
+        assert torch.equal(v.cpu(), sep[k]), k
+    assert torch.count_nonzero(ws1).item() == 0 and torch.count_nonzero(ws2).item() == 0
+
+
 def test_block_rejects_fp8_and_missing_workspace():
     import gemm_epilogue_fusion_gb300 as g
     X = torch.zeros(128, 128, dtype=torch.uint8, device="cuda")
