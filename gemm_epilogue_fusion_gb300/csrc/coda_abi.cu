@@ -103,6 +103,12 @@ coda_status check_gemm_dims(int64_t M, int64_t N, int64_t K, coda_dtype dt, cons
           16 / elem_bytes(dt));
   REQUIRE((N * out_bytes(dt)) % 16 == 0, "%s = %" PRId64 " must be a multiple of %d for this dtype (16-byte rows)",
           nname, N, 16 / out_bytes(dt));
+  // byte extents of every operand must fit int64, and the kernels' tile
+  // indices are 32-bit: bound both at the smallest tile, 128 x 128 outputs
+  REQUIRE(M * N < (int64_t(1) << 60) && M * K < (int64_t(1) << 60) && N * K < (int64_t(1) << 60),
+          "M = %" PRId64 ", %s = %" PRId64 ", K = %" PRId64 ": a matrix of 2^60 elements or more", M, nname, N, K);
+  REQUIRE(((M + 127) / 128) * ((N + 127) / 128) < INT32_MAX / 2,
+          "M = %" PRId64 ", %s = %" PRId64 ": too many output tiles for the kernels' 32-bit tile indices", M, nname, N);
   return CODA_OK;
 }
 

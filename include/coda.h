@@ -43,7 +43,8 @@
  *     output width must be multiples of 4 (CODA_F32), 8 (CODA_BF16) or 16
  *     (CODA_E4M3 operands).
  *   - Sizes are int64_t; M may be 0 (nothing is launched), N and K must be
- *     positive; every dimension must be below 2^31.
+ *     positive; every dimension must be below 2^31, every matrix below 2^60
+ *     elements, and a GEMM below 2^30 output tiles of 128 x 128.
  *   - Ownership: the caller owns all memory.  The library never allocates,
  *     frees or synchronises; every call only enqueues work on `stream`
  *     (cudaStream_t; NULL = the legacy default stream) and returns.

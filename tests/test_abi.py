@@ -68,6 +68,15 @@ def test_rejects_bad_shapes(lib):
     assert _rpr(lib, dt=7) == g.CODA_ERR_INVALID_ARG
 
 
+def test_rejects_sizes_beyond_32_bit_tile_indices(lib):
+    # plausible-looking but absurd sizes are refused before anything is enqueued
+    big = (1 << 31) - 8
+    assert _rpr(lib, M=big, N=big, K=8) == g.CODA_ERR_INVALID_ARG
+    assert b"2^60" in lib.coda_last_error() or b"tile" in lib.coda_last_error()
+    assert _rpr(lib, M=1 << 30, N=1 << 20, K=8) == g.CODA_ERR_INVALID_ARG
+    assert b"tile" in lib.coda_last_error()
+
+
 def test_rejects_overlapping_outputs(lib):
     assert _rpr(lib, H=A + 128 * MB) == g.CODA_ERR_INVALID_ARG   # h over R
     assert b"overlaps input R" in lib.coda_last_error()
