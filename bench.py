@@ -616,6 +616,14 @@ def run_coda(args, w):
         line["cpu_baseline"] = {"value": fl_cpu / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                 "sample": f"first {n} of {w.M} rows of the same batch (rows are independent), "
                                           f"{dt:.1f} s of fp64 unfused oracle"}
+        # the same oracle on one core, on a smaller sample
+        import oracle
+        prev = oracle.set_threads(0)
+        oracle.set_threads(1)
+        n1, dt1, fl1, _ = oracle_sample(w, inp, args.cpu_budget / 4)
+        oracle.set_threads(prev)
+        line["cpu_baseline"]["value_1thread"] = fl1 / dt1 / 1e12
+        line["cpu_baseline"]["sample_1thread"] = f"first {n1} rows, {dt1:.1f} s on one thread"
     print(json.dumps(line), flush=True)
 
 

@@ -76,6 +76,8 @@ def _load():
             lib.coda_oracle_e4m3_fake_quant.restype = ctypes.c_double
             lib.coda_oracle_rmsnorm_backward.argtypes = [_dp, _dp, ctypes.c_double, _dp, _i64, _i64, _dp, _dp]
             lib.coda_oracle_silu_mul_backward.argtypes = [_dp, _dp, _dp, _i64, _dp, _dp]
+            lib.coda_oracle_threads.argtypes = [ctypes.c_int]
+            lib.coda_oracle_threads.restype = ctypes.c_int
             lib.coda_oracle_rope.argtypes = [_dp, _i64, _i64, _i64, _i64, ctypes.POINTER(ctypes.c_int64),
                                              ctypes.c_double]
             _lib = lib
@@ -93,6 +95,12 @@ def _ptr(a: np.ndarray):
 
 
 # ---------------------------------------------------------------- steps ----
+
+def set_threads(n: int) -> int:
+    """Threads of the oracle's OpenMP loops (n > 0 sets it); returns the count in
+    effect.  Only for timing: results do not depend on it."""
+    return int(_load().coda_oracle_threads(int(n)))
+
 
 def gemm(A, W, R=None) -> np.ndarray:
     """C = R + A.W (R optional).  A [M,K], W [K,N]."""

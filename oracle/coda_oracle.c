@@ -21,6 +21,23 @@
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Thread count of the OpenMP loops below (n > 0 sets it; n <= 0 leaves it);
+ * returns the count in effect.  For timing the oracle on one core: the
+ * arithmetic and its order within each output element do not depend on it. */
+int coda_oracle_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 /* C = R + A . W   (R may be NULL, meaning zero).
  * A [M x K], W [K x N], R and C [M x N].  i-k-j loops, fp64 accumulate.
