@@ -1035,9 +1035,9 @@ cudaError_t launch_gemm(const GemmProblem& p, const char** msg) {
         return cudaErrorInvalidValue;
       }
       if (p.epi == kEpiGradNorm)
-        return pair ? launch_cfg<GemmCfg<KIND, kEpiGradNorm, kNoPhase, 5, 4, 2, false, true>>(p, msg)
+        return pair ? launch_cfg<GemmCfg<KIND, kEpiGradNorm, kNoPhase, 6, 2, 2, false, true>>(p, msg)
                     : launch_cfg<GemmCfg<KIND, kEpiGradNorm, kNoPhase, 3, 4, 1, false, true>>(p, msg);
-      return pair ? launch_cfg<GemmCfg<KIND, kEpiSwiGLUBwd, kNoPhase, 5, 4, 2, false, true>>(p, msg)
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiSwiGLUBwd, kNoPhase, 6, 2, 2, false, true>>(p, msg)
                   : launch_cfg<GemmCfg<KIND, kEpiSwiGLUBwd, kNoPhase, 3, 4, 1, false, true>>(p, msg);
     }
     // MN-major operands (transposed products of the backward pass): row-scale program
