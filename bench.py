@@ -710,6 +710,18 @@ def run_coda_backward(args, w):
         "gpu_launches": 12 * args.steps, "clocks": clk.summary()}), flush=True)
 
 
+def _compile_toolchain():
+    """torch.compile's Triton kernels need a ptxas that knows this GPU's
+    architecture; Triton's bundled one may predate it, so use the CUDA
+    toolkit's unless the caller chose one."""
+    if "TRITON_PTXAS_PATH" not in os.environ:
+        for root in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+            cand = os.path.join(root, "bin", "ptxas") if root else None
+            if cand and os.path.exists(cand):
+                os.environ["TRITON_PTXAS_PATH"] = cand
+                break
+
+
 def run_unfused_backward(args, w):
     """PyTorch eager autograd through the unfused chain (cuBLAS GEMMs, fp32-math
     RMSNorm, silu * mul), backward only."""
@@ -736,6 +748,8 @@ def run_unfused_backward(args, w):
         Z = rms(h2, G["gamma2"]) @ P["Wqt"].t()
         return Z, h2
 
+    if args.compile:
+        _compile_toolchain()
     fwd = torch.compile(forward_fn) if args.compile else forward_fn
 
     def step():
@@ -782,6 +796,7 @@ def run_unfused(args, w):
         return h, torch.nn.functional.silu(g_) * u
 
     if args.compile:
+        _compile_toolchain()
         step = torch.compile(step)
 
     for _ in range(args.warmup):
