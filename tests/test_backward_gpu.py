@@ -116,6 +116,45 @@ def test_chain_backward_llama8b_full_size_sampled_rows():
     print(_check(got, ref, [p for p in CHAIN_PAIRS if p[0] in ("dX", "dR", "dh2", "dG", "dU")], rows=rows))
 
 
+def test_chain_backward_llama8b_full_size_weight_gradients():
+    """M = 16384, the launch configuration bench.py times: each weight gradient
+    (and dX) is a transposed product over all 16384 rows, which the row-sampled
+    oracle cannot see.  Each is checked against an fp32 product of the very
+    bf16 operands the backward fed its kernel, at the parity bar."""
+    import gemm_epilogue_fusion_gb300 as g
+    from gemm_epilogue_fusion_gb300 import chain as C
+    w = WORKLOADS["llama8b_chain"]
+    inp = make_inputs(w)
+    d = to_device(inp)
+    gen = torch.Generator(device="cuda").manual_seed(87)
+    dZ = torch.randn(w.M, w.N2, generator=gen, device="cuda").bfloat16()
+    f = C.fold_weights("full", {k: d[k] for k in d if k.startswith("W")}, {k: d[k] for k in d if k.startswith("gamma")})
+    fwd = C.full_chain_train_forward(d["X"], d["W1t"], d["R"], f["Wgt"], f["Wut"], d["Wdt"], f["Wqt"], w.eps)
+    Wgut = torch.cat([d["Wgt"], d["Wut"]], 0).contiguous()
+    g1, g2 = d["gamma1"], d["gamma2"]
+    # the backward's steps, keeping every operand of its weight-gradient products
+    dy2, S2 = g.coda_gemm_grad_norm(dZ, d["Wqt"], fwd["h2"], g2)
+    dh2, Yt2, _ = g.coda_rmsnorm_backward(dy2, fwd["h2"], fwd["r2"], g2, S2)
+    dGU = g.coda_gemm_swiglu_backward(dh2, d["Wdt"], fwd["GU"])
+    dy1, S1 = g.coda_gemm_grad_norm(dGU, Wgut, fwd["h1"], g1)
+    dh1, Yt1, _ = g.coda_rmsnorm_backward(dy1, fwd["h1"], fwd["r1"], g1, S1, dh2)
+    got = {"dWqt": g.coda_gemm(dZ, Yt2, a_mn=True, b_mn=True, col_scale=g2),
+           "dWdt": g.coda_gemm(dh2, fwd["act"], a_mn=True, b_mn=True),
+           "dWgut": g.coda_gemm(dGU, Yt1, a_mn=True, b_mn=True, col_scale=g1),
+           "dWot": g.coda_gemm(dh1, d["X"], a_mn=True, b_mn=True),
+           "dX": g.coda_gemm(dh1, d["W1t"], b_mn=True)}
+    ref = {"dWqt": (dZ.float().t() @ Yt2.float()) * g2,
+           "dWdt": dh2.float().t() @ fwd["act"].float(),
+           "dWgut": (dGU.float().t() @ Yt1.float()) * g1,
+           "dWot": dh1.float().t() @ d["X"].float(),
+           "dX": dh1.float() @ d["W1t"].float()}
+    torch.cuda.synchronize()
+    errs = {k: float((got[k].float() - ref[k]).abs().max() / (ref[k].abs().max() + 1e-6)) for k in got}
+    print(errs)
+    assert all(e <= TOL["bf16"] for e in errs.values()), errs
+    assert g.coda_get_device_status() == g.CODA_OK
+
+
 @pytest.mark.parametrize("cg", ["1", "2"])
 def test_swiglu_save_matches_plain_forward_and_oracle(cg, monkeypatch):
     """The saving forward's act equals coda_gemm_swiglu_fused_rms bit for bit,
