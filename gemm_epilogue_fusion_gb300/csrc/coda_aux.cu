@@ -31,29 +31,36 @@ __global__ void __launch_bounds__(256) rms_reduce_kernel(const float* __restrict
   r[i] = row_rstd(P + static_cast<int64_t>(i) * T, T, n, eps);
 }
 
-// 16 bytes of W^T per thread: 8 bf16 or 4 fp32 elements of one row (K gives
-// 16-byte rows, so a vector never straddles two rows).
+// One 16-byte vector of W^T per thread and row: 8 bf16 or 4 fp32 elements.
+// Thread x of the grid owns the vector column x (K gives 16-byte rows, so a
+// vector never straddles two rows), loads its gamma once, and walks the rows
+// blockIdx.y, blockIdx.y + gridDim.y, ...
 template <bool F32>
 __global__ void __launch_bounds__(256) fold_gamma_kernel(const uint4* __restrict__ W, const float* __restrict__ gamma,
-                                                         uint4* __restrict__ out, int64_t n_vec, int64_t K) {
+                                                         uint4* __restrict__ out, int64_t n_rows, int64_t row_vecs) {
   constexpr int VEC = F32 ? 4 : 8;
-  for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < n_vec;
-       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t k0 = (v * VEC) % K;
-    uint4 w = W[v];
+  const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (c >= row_vecs) return;
+  float g[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) g[e] = __ldg(gamma + c * VEC + e);
+#pragma unroll 4
+  for (int64_t r = blockIdx.y; r < n_rows; r += gridDim.y) {
+    const int64_t v = r * row_vecs + c;
+    uint4 w = __ldg(W + v);
     if constexpr (F32) {
       float4 f = *reinterpret_cast<float4*>(&w);
-      f.x *= gamma[k0];
-      f.y *= gamma[k0 + 1];
-      f.z *= gamma[k0 + 2];
-      f.w *= gamma[k0 + 3];
+      f.x *= g[0];
+      f.y *= g[1];
+      f.z *= g[2];
+      f.w *= g[3];
       out[v] = *reinterpret_cast<uint4*>(&f);
     } else {
       __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 f = __bfloat1622float2(h[e]);
-        h[e] = __floats2bfloat162_rn(f.x * gamma[k0 + 2 * e], f.y * gamma[k0 + 2 * e + 1]);
+        h[e] = __floats2bfloat162_rn(f.x * g[2 * e], f.y * g[2 * e + 1]);
       }
       out[v] = w;
     }
@@ -343,14 +350,19 @@ cudaError_t launch_rms_reduce(const float* P, int64_t M, int T, int64_t N, float
 
 cudaError_t launch_fold_gamma(const void* Wt, const float* gamma, void* Wt_out, int64_t N_out, int64_t K, bool f32,
                               cudaStream_t s) {
-  const int64_t n_vec = N_out * K / (f32 ? 4 : 8);
-  const int g = grid_for(n_vec, 256);
+  const int64_t row_vecs = K / (f32 ? 4 : 8);
+  const unsigned gx = static_cast<unsigned>((row_vecs + 255) / 256);
+  // about 8 blocks per SM in all, each walking every gridDim.y-th row
+  int64_t gy = (static_cast<int64_t>(device_sm_count()) * 8 + gx - 1) / gx;
+  gy = gy < N_out ? gy : N_out;
+  gy = gy < 65535 ? gy : 65535;
+  const dim3 grid(gx, static_cast<unsigned>(gy > 0 ? gy : 1));
   if (f32)
-    fold_gamma_kernel<true><<<g, 256, 0, s>>>(static_cast<const uint4*>(Wt), gamma, static_cast<uint4*>(Wt_out),
-                                              n_vec, K);
+    fold_gamma_kernel<true><<<grid, 256, 0, s>>>(static_cast<const uint4*>(Wt), gamma, static_cast<uint4*>(Wt_out),
+                                                 N_out, row_vecs);
   else
-    fold_gamma_kernel<false><<<g, 256, 0, s>>>(static_cast<const uint4*>(Wt), gamma, static_cast<uint4*>(Wt_out),
-                                               n_vec, K);
+    fold_gamma_kernel<false><<<grid, 256, 0, s>>>(static_cast<const uint4*>(Wt), gamma, static_cast<uint4*>(Wt_out),
+                                                  N_out, row_vecs);
   return cudaGetLastError();
 }
 

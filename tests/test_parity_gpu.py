@@ -123,3 +123,20 @@ def test_row_scale_invariance_heavy_rows():
     sc = run_gpu(w, d2)
     assert oracle.rel_err(sc["Z"], base["Z"]) < 1e-2
     np.testing.assert_allclose(sc["r"].numpy() * 50, base["r"].numpy(), rtol=1e-2)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", [(1, 8), (3, 24), (257, 520), (14336, 4096)])
+def test_fold_gamma_bit_exact(dtype, shape):
+    """W'^T = W^T diag(gamma), each product in fp32 then rounded once: equal,
+    bit for bit, to the same product rounded by torch (ragged row counts,
+    one-vector rows, and the 8B gate weight's full size)."""
+    import gemm_epilogue_fusion_gb300 as g
+    if dtype == torch.float32 and shape[1] % 4:
+        pytest.skip("fp32 rows of 16 bytes need K % 4 == 0")
+    gen = torch.Generator(device="cuda").manual_seed(sum(shape))
+    W = torch.randn(*shape, generator=gen, device="cuda").to(dtype)
+    gam = torch.rand(shape[1], generator=gen, device="cuda") + 0.5
+    out = g.coda_fold_gamma(W, gam)
+    torch.cuda.synchronize()
+    assert torch.equal(out, (W.float() * gam).to(dtype))
