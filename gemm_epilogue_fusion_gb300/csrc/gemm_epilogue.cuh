@@ -64,9 +64,13 @@
 namespace coda {
 
 // Tuning: rows of one raster band (consecutive tiles walk the band's M-tiles
-// before moving right) and the L2 eviction policy of the A and B operand loads.
+// before moving right), for the SwiGLU programs and for the others, and the
+// L2 eviction policy of the A and B operand loads.
 #ifndef CODA_RASTER_ROWS
 #define CODA_RASTER_ROWS 2048
+#endif
+#ifndef CODA_RASTER_ROWS_SWIGLU
+#define CODA_RASTER_ROWS_SWIGLU 4096
 #endif
 #ifndef CODA_L2_POLICY_A
 #define CODA_L2_POLICY_A l2_policy_evict_last()
@@ -85,6 +89,16 @@ constexpr int kNoPhase = -1;
 
 // Programs whose B tile is gate rows ++ up rows (N = 128 + 128).
 __host__ __device__ constexpr bool is_swiglu(int epi) { return epi == kEpiSwiGLU || epi == kEpiSwiGLUSave; }
+// Rows of one raster band of a program's tiles.  Each band reads every weight
+// panel of the phase once (and its own activation panels from L2), so a wider
+// band re-reads the weights fewer times, as long as the band's panels still
+// fit in L2.  A SwiGLU tile reads two weight panels (gate and up) per output
+// column block, so its weights dominate: 4096-row bands cut the weight
+// re-reads in half.  For the other programs the weights are small against
+// the activations and 2048-row bands measure faster.
+__host__ __device__ constexpr int raster_rows(int epi) {
+  return is_swiglu(epi) ? CODA_RASTER_ROWS_SWIGLU : CODA_RASTER_ROWS;
+}
 
 template <int KIND, int EPI_A, int EPI_B, int STAGES_, int NSLOTS_, int CG_ = 1, bool A_MN_ = false,
           bool B_MN_ = false>
@@ -131,7 +145,6 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int NUM_EPI_THREADS = 128;
   static constexpr int NUM_THREADS = HAS_LOADER ? 224 : 192;
-  static constexpr int GROUP_M = CODA_RASTER_ROWS / TILE_M;  // tile raster: row bands sharing each B panel
   // shared memory: [A stages][B stages][slots][barriers][tmem slot, abort flag]
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SLOTS = OFF_B + STAGES * B_BYTES;
@@ -160,15 +173,14 @@ struct TileCoord {
   int m, n;
 };
 
-// Grouped raster: consecutive tile indices walk GROUP_M M-tiles down one
+// Grouped raster: consecutive tile indices walk group_m M-tiles down one
 // column of output tiles before moving right, so the CTAs in flight share a
 // few A and B panels in L2.
-template <int GROUP_M>
-__device__ __forceinline__ TileCoord tile_coord(int t, int m_tiles, int n_tiles) {
-  const int per_group = GROUP_M * n_tiles;
+__device__ __forceinline__ TileCoord tile_coord(int t, int m_tiles, int n_tiles, int group_m) {
+  const int per_group = group_m * n_tiles;
   const int g = t / per_group;
-  const int first_m = g * GROUP_M;
-  const int gm = min(GROUP_M, m_tiles - first_m);
+  const int first_m = g * group_m;
+  const int gm = min(group_m, m_tiles - first_m);
   const int local = t - g * per_group;
   return {first_m + local % gm, local / gm};
 }
@@ -178,14 +190,13 @@ struct Tile {
   int phase;  // 0 = A, 1 = B
   int m, n;
 };
-template <int GROUP_M>
-__device__ __forceinline__ Tile tile_at(int t, int m_tiles, int n_tiles_a, int n_tiles_b) {
+__device__ __forceinline__ Tile tile_at(int t, int m_tiles, int n_tiles_a, int n_tiles_b, int group_a, int group_b) {
   const int num_a = m_tiles * n_tiles_a;
   if (t < num_a) {
-    const TileCoord c = tile_coord<GROUP_M>(t, m_tiles, n_tiles_a);
+    const TileCoord c = tile_coord(t, m_tiles, n_tiles_a, group_a);
     return {0, c.m, c.n};
   }
-  const TileCoord c = tile_coord<GROUP_M>(t - num_a, m_tiles, n_tiles_b);
+  const TileCoord c = tile_coord(t - num_a, m_tiles, n_tiles_b, group_b);
   return {1, c.m, c.n};
 }
 
@@ -294,6 +305,7 @@ __device__ __forceinline__ bool wait_band(const unsigned* ctr, unsigned target, 
 struct PhaseArgs {
   int N_out, K;
   EpiParams ep;
+  int group_m;  // M-tiles per raster band (>= 1)
 };
 
 template <class C>
@@ -434,7 +446,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       for (int k = 0; ok; ++k) {
         const int t = walk(k);
         if (t >= num_tiles) break;
-        const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
+        const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.group_m, pb.group_m);
         const int num_kb = num_kb_of(tl);
         if (C::TWO_PHASE && tl.phase == 1) {
           // h and P of this band come from other CTAs of this launch
@@ -483,7 +495,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       for (int k = 0; ok; ++k, ++it) {
         const int t = walk(k);
         if (t >= num_tiles) break;
-        const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
+        const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.group_m, pb.group_m);
         const int num_kb = (((C::TWO_PHASE && tl.phase == 1) ? pb.K : pa.K) + C::BK - 1) / C::BK;
         const int buf = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
@@ -532,7 +544,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         for (int k = 0; ok; ++k) {
           const int t = walk(k);
           if (t >= num_tiles) break;
-          const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
+          const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.group_m, pb.group_m);
           const bool pB = C::TWO_PHASE && tl.phase == 1;
           const int row0 = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
           if (row0 >= M) continue;  // this CTA's half of the tile is empty
@@ -850,7 +862,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     for (int k = 0; ok; ++k, ++it) {
       const int t = walk(k);
       if (t >= num_tiles) break;
-      const Tile tl = tile_at<C::GROUP_M>(t, m_tiles, n_tiles_a, n_tiles_b);
+      const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.group_m, pb.group_m);
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
       // one decision for all 128 threads, so no thread is left at a barrier
@@ -998,8 +1010,10 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
   // grid never exceeds the co-resident units
   const int grid = C::CG * (num_tiles < units ? num_tiles : units);
   int M = p.M;
-  PhaseArgs pa = {p.N_out, p.K, p.ep};
-  PhaseArgs pb = {p.b.N_out, p.b.K, p.b.ep};
+  constexpr int group_a = raster_rows(C::kEpiA) / C::TILE_M > 0 ? raster_rows(C::kEpiA) / C::TILE_M : 1;
+  constexpr int group_b = raster_rows(C::kEpiB) / C::TILE_M > 0 ? raster_rows(C::kEpiB) / C::TILE_M : 1;
+  PhaseArgs pa = {p.N_out, p.K, p.ep, group_a};
+  PhaseArgs pb = {p.b.N_out, p.b.K, p.b.ep, group_b};
   unsigned* band_ready = p.band_ready;
   void* args[] = {&tmA, &tmB, &tmB2, &tmR, &tmD, &tmA_b, &tmB_b, &tmB2_b, &tmD_b, &M, &pa, &pb, &band_ready};
   ce = launch_ex(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(C::NUM_THREADS), C::SMEM_BYTES, p.stream,
