@@ -176,7 +176,7 @@ struct TileCoord {
 // Grouped raster: consecutive tile indices walk group_m M-tiles down one
 // column of output tiles before moving right, so the CTAs in flight share a
 // few A and B panels in L2.
-__device__ __forceinline__ TileCoord tile_coord(int t, int m_tiles, int n_tiles, int group_m) {
+__host__ __device__ __forceinline__ TileCoord tile_coord(int t, int m_tiles, int n_tiles, int group_m) {
   const int per_group = group_m * n_tiles;
   const int g = t / per_group;
   const int first_m = g * group_m;
@@ -190,7 +190,8 @@ struct Tile {
   int phase;  // 0 = A, 1 = B
   int m, n;
 };
-__device__ __forceinline__ Tile tile_at(int t, int m_tiles, int n_tiles_a, int n_tiles_b, int group_a, int group_b) {
+__host__ __device__ __forceinline__ Tile tile_at(int t, int m_tiles, int n_tiles_a, int n_tiles_b, int group_a,
+                                                  int group_b) {
   const int num_a = m_tiles * n_tiles_a;
   if (t < num_a) {
     const TileCoord c = tile_coord(t, m_tiles, n_tiles_a, group_a);

@@ -3,7 +3,9 @@ the host: compiled from the kernel header itself with nvcc and run on the CPU.
 Every tile index is dealt exactly once, each unit's walk increases, every unit
 walks all its phase-A tiles before any phase-B tile (what keeps the
 two-phase launch's band waits free of cycles), and on the workloads' shapes the
-busiest unit gets no more k-blocks than under a plain round robin."""
+busiest unit gets no more k-blocks than under a plain round robin.  The
+grouped raster (tile_at) maps the tile indices of each phase one to one onto
+its grid of output tiles for every band width, ragged last bands included."""
 import os
 import shutil
 import subprocess
@@ -19,6 +21,20 @@ PROGRAM = r"""
 #include <vector>
 #include <algorithm>
 using coda::walk_tile;
+using coda::tile_at;
+// 0 if tile_at maps phase A's and phase B's indices one to one onto their grids
+static int check_raster(int m_tiles, int n_a, int n_b, int g_a, int g_b) {
+  std::vector<int> seen_a(m_tiles * n_a, 0), seen_b(m_tiles * n_b, 0);
+  for (int t = 0; t < m_tiles * (n_a + n_b); ++t) {
+    const coda::Tile c = tile_at(t, m_tiles, n_a, n_b, g_a, g_b);
+    const int nn = c.phase ? n_b : n_a;
+    if (c.phase != (t >= m_tiles * n_a) || c.m < 0 || c.m >= m_tiles || c.n < 0 || c.n >= nn) return 1;
+    (c.phase ? seen_b : seen_a)[c.m * nn + c.n]++;
+  }
+  for (int v : seen_a) if (v != 1) return 2;
+  for (int v : seen_b) if (v != 1) return 2;
+  return 0;
+}
 static int d_of(int kb_a, int kb_b) { return (kb_a + kb_b / 2) / std::max(1, kb_b); }
 // 0 if every tile is dealt once, walks increase and phase A precedes phase B
 static int check_cover(int U, int nA, int nB, int d, long* max_w, long* max_rr, int kb_a, int kb_b) {
@@ -43,6 +59,12 @@ static int check_cover(int U, int nA, int nB, int d, long* max_w, long* max_rr, 
 }
 int main() {
   long w, rr;
+  for (int m = 1; m <= 40; m += 3)
+    for (int na = 1; na <= 24; na += 5)
+      for (int nb = 0; nb <= 70; nb += 23)
+        for (int ga = 1; ga <= 34; ga += 3)
+          for (int gb = 1; gb <= 34; gb += 4)
+            if (check_raster(m, na, nb, ga, gb)) { printf("FAIL raster m=%d na=%d nb=%d ga=%d gb=%d\n", m, na, nb, ga, gb); return 1; }
   for (int U = 1; U < 160; U += 3)
     for (int nA = 0; nA < 700; nA += 41)
       for (int nB = 0; nB < 900; nB += 67)
