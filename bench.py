@@ -2,27 +2,33 @@
 
 Default workload: the LLaMA-3-1B attention-out block, bf16 in / fp32
 accumulate, M = 8192 tokens (batch 4 x seq 2048):
-    h = R + X Wo            X [8192, 2048], Wo [2048, 2048]   coda_gemm_residual_partial_rms
-    r = rms(h)                                                 coda_rms_reduce
-    act = SwiGLU(r h Wg', r h Wu')   Wg, Wu [2048, 8192]       coda_gemm_swiglu
-One step = one pass of that chain over one batch: 2 kernel launches with the
-reduction folded into the SwiGLU GEMM's epilogue (default), 3 with
-``--reduce separate``.
+    h = R + X Wo            X [8192, 2048], Wo [2048, 2048]   residual + partial RMS program
+    r = rms(h)                                                 reduction, in the consumer's epilogue
+    act = SwiGLU(r h Wg', r h Wu')   Wg, Wu [2048, 8192]       SwiGLU program
+One step = one pass of that chain over one batch.  The default
+``--reduce block`` runs it as one two-phase launch (coda_block_swiglu);
+``--reduce fused`` as 2 launches (coda_gemm_residual_partial_rms, then
+coda_gemm_swiglu_fused_rms); ``--reduce separate`` as 3 (coda_rms_reduce
+between them).  ``--workload`` selects the other configurations and
+``--pass backward|aux`` the backward chain or the memory-bound kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl coda|reference|unfused]
 
 Prints ONE JSON line (rank 0).  ``value`` is the whole-job TFLOP/s with
-inputs resident in HBM (3 rotating input sets of 136 MB each, so every step
-reads inputs that are not in the 129 MB L2); ``e2e`` is the same metric
-with the inputs copied in from pinned host memory and h and act copied back
-every step (copies of one step overlapped with the compute of the next); ``roofline`` is the SwiGLU GEMM (89% of the flops) timed live
-with CUDA events around each of its launches; ``cpu_baseline`` is the fp64
-CPU oracle timed on this host on a bounded row sample.  Multi-GPU: one
-process per GPU (torchrun), each rank runs its own independent batch (weak
-scaling, no collective on the data path; a barrier and a max-reduce of the
-elapsed time bracket the timed region).
-``--impl reference`` times the CPU oracle alone; ``--impl unfused`` times the
-unfused PyTorch sequence (cuBLAS GEMM, add, RMSNorm, GEMM, silu*mul).
+inputs resident in HBM (3 rotating sets of X, R and the weights, 143 MB
+each for the default workload, so every step reads inputs that are not in
+the 129 MB L2); ``e2e`` is the same metric with X and R copied in from
+pinned host memory and h and act copied back every step (copies of one step
+overlapped with the compute of its neighbours); ``roofline`` is the
+dominant kernel (the block kernel by default; the SwiGLU GEMM, 89% of the
+flops, with ``--reduce fused``) timed live with CUDA events around each of
+its launches; ``cpu_baseline`` is the fp64 CPU oracle timed on this host on
+a bounded row sample.  Multi-GPU: one process per GPU (torchrun), each rank
+runs its own independent batch (weak scaling, no collective on the data
+path; a barrier and a max-reduce of the elapsed time bracket the timed
+region).  ``--impl reference`` times the CPU oracle alone; ``--impl
+unfused`` times the unfused PyTorch sequence (cuBLAS GEMM, add, RMSNorm,
+GEMM, silu*mul), ``--compile`` the same under torch.compile.
 """
 from __future__ import annotations
 
