@@ -240,8 +240,21 @@ def oracle_sample(w, inp, budget_s, min_rows=16, max_rows=8192):
     t = timed(min_rows)
     n = int(max(min_rows, min(max_rows, w.M, budget_s / max(t, 1e-6) * min_rows)))
     dt = timed(n)
-    threads = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
-    return n, dt, per_row_flops(w) * n, threads
+    import oracle
+    return n, dt, per_row_flops(w) * n, oracle.set_threads(0)
+
+
+def cpu_model():
+    """The host CPU's model name, as lscpu prints it, for the oracle baseline's
+    record (the machine type if lscpu is missing)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return os.uname().machine
 
 
 # -------------------------------------------------------------- the arms ----
@@ -252,7 +265,8 @@ def run_reference(args, w):
         return
     inp = make_inputs(w)
     run = oracle_runner(w, inp)
-    threads = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    import oracle
+    threads = oracle.set_threads(0)
     # size each step's row sample so that warm-up + timed steps end in about
     # --ref-budget seconds, with at least one row per thread
     t0 = time.perf_counter()
@@ -273,7 +287,7 @@ def run_reference(args, w):
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, "separate"),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "cpu": cpu_model(),
                          "sample": f"{rows} rows of the {w.M}-row batch per step (rows are independent), "
                                    f"fp64 unfused oracle"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -620,6 +634,7 @@ def run_coda(args, w):
     if not args.no_cpu_baseline:
         n, dt, fl_cpu, threads = oracle_sample(w, inp, args.cpu_budget)
         line["cpu_baseline"] = {"value": fl_cpu / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "cpu": cpu_model(),
                                 "sample": f"first {n} of {w.M} rows of the same batch (rows are independent), "
                                           f"{dt:.1f} s of fp64 unfused oracle"}
         # the same oracle on one core, on a smaller sample
