@@ -56,3 +56,37 @@ def test_noalloc_rejects_rows_beyond_its_counters():
     st = lib.coda_block_swiglu_noalloc(A, A, A, A, A, 1e-5, A, A, None, A, 131073, 512, 512, 512, 1, None)
     assert st == g.CODA_ERR_INVALID_ARG
     assert b"131072" in lib.coda_last_error()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_noalloc_block_at_its_row_limit(cg, monkeypatch):
+    """M = 131072, the most rows the built-in counters serve.  With one CTA per
+    tile the launch uses every one of them (1024 bands of 128 rows and the
+    completion counter).  The outputs equal the workspace form bit for bit, and
+    sampled rows (the first, the last, and the rows of the last two bands)
+    match the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gemm_epilogue_fusion_gb300 as g
+    from coda_inputs import sample_rows
+    monkeypatch.setenv("CODA_CTA_GROUP", cg)
+    g.load_library()
+    w = Workload("noalloc_max", "swiglu", 131072, 256, 256, 256, 0, "bf16", 1e-5, 63)
+    inp = make_inputs(w)
+    d = {k: v.cuda() for k, v in inp.items()}
+    Wg = g.coda_fold_gamma(d["Wgt"], d["gamma1"])
+    Wu = g.coda_fold_gamma(d["Wut"], d["gamma1"])
+    ws = g.block_workspace(w.M, "cuda")
+    ref = g.coda_block_swiglu(d["X"], d["W1t"], d["R"], Wg, Wu, w.eps, ws)
+    got = g.coda_block_swiglu_noalloc(d["X"], d["W1t"], d["R"], Wg, Wu, w.eps)
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    rows = torch.cat([sample_rows(w.M, 8), torch.arange(w.M - 256, w.M, 37)]).unique()
+    Wt = lambda t: t.double().numpy().T.copy()  # noqa: E731
+    o = oracle.block_swiglu(inp["X"][rows], Wt(inp["W1t"]), inp["R"][rows], inp["gamma1"], Wt(inp["Wgt"]),
+                            Wt(inp["Wut"]), w.eps)
+    assert oracle.rel_err(got[0].cpu()[rows], o["h"]) <= TOL
+    assert oracle.rel_err(got[2].cpu()[rows], o["act"]) <= TOL
+    assert g.coda_get_device_status() == g.CODA_OK
