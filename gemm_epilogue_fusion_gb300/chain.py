@@ -12,7 +12,12 @@ epilogue"; SwiGLU gate/up from the same section and "five blocks"):
                   h1 = R + X Wo ; r1 ; act = SwiGLU(r1, h1) ;
                   h2 = h1 + act Wd ; r2 ; Z = diag(r2) h2 Wq'          (6 launches)
   full_chain_fp8  the same with every GEMM operand in per-tensor-scaled e4m3
+  full_chain_train_forward / full_chain_backward, rowscale_block_backward
+                  the training forward that saves G || U and r, and the
+                  backward from that state (12 launches for the full chain)
 W' = diag(gamma) W is prepared once by ``fold_weights`` (coda_fold_gamma).
+The one-launch forms of the two blocks are the binding's coda_block_rowscale
+and coda_block_swiglu themselves.
 With ``fused_reduce=True`` the reduction of the partials to r runs inside the
 consuming GEMM's epilogue (coda_gemm_*_fused_rms) instead of its own launch;
 r is still written out.
