@@ -193,6 +193,9 @@ def dist_setup(backend):
     if ws > 1:
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        if backend == "nccl":
+            # this rank's GPU first, so NCCL's communicators bind to it
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group(backend=backend)
         return dist, dist.get_rank(), ws
     return None, 0, 1
