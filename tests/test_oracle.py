@@ -254,6 +254,29 @@ def test_rope_first_pair_turns_by_the_position_in_every_head():
         assert got[0, c + 1] == pytest.approx(math.sin(1.0), abs=1e-15)   # counter-clockwise
 
 
+def test_block_rowscale_rope_rotates_only_the_qk_columns_of_the_block():
+    """The composed oracle (block, then RoPE on the QKV output): at position 0
+    it is the plain block; the columns past rot_cols (V) equal the plain
+    block's at any position; every rotated pair keeps its length; and the
+    first pair of each head turns by exactly p radians (theta_0 = 1)."""
+    rng = np.random.default_rng(12)
+    M, K, N, N2, rot, d = 5, 24, 16, 40, 32, 8
+    X, R = rng.standard_normal((M, K)), rng.standard_normal((M, N))
+    W1, W2 = rng.standard_normal((K, N)) / K ** 0.5, rng.standard_normal((N, N2)) / N ** 0.5
+    gamma = 1 + 0.1 * rng.standard_normal(N)
+    plain = oracle.block_rowscale(X, W1, R, gamma, W2, 1e-5)["Z"]
+    at_zero = oracle.block_rowscale_rope(X, W1, R, gamma, W2, 1e-5, rot, d, np.zeros(M), 500000.0)["Z"]
+    np.testing.assert_array_equal(at_zero, plain)
+    pos = np.array([1, 2, 17, 300, 4095])
+    got = oracle.block_rowscale_rope(X, W1, R, gamma, W2, 1e-5, rot, d, pos, 500000.0)["Z"]
+    np.testing.assert_array_equal(got[:, rot:], plain[:, rot:])
+    np.testing.assert_allclose(np.hypot(got[:, 0:rot:2], got[:, 1:rot:2]),
+                               np.hypot(plain[:, 0:rot:2], plain[:, 1:rot:2]), rtol=1e-12)
+    for c in range(0, rot, d):
+        turn = np.arctan2(got[:, c + 1], got[:, c]) - np.arctan2(plain[:, c + 1], plain[:, c]) - pos
+        np.testing.assert_allclose(np.mod(turn + np.pi, 2 * np.pi) - np.pi, 0, atol=1e-9)
+
+
 def test_rope_scores_depend_only_on_relative_position():
     rng = np.random.default_rng(10)
     d = 16
