@@ -1,7 +1,8 @@
 """CPU oracle for the CODA GEMM-epilogue block -- TEST INFRASTRUCTURE ONLY.
 
-Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` may import this package.  The CUDA product path never does.
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg and ``--impl reference`` arm may import this package.  The CUDA product
+path never does.
 
 What it computes is the *plain, unfused* definition of the block that the CODA
 news write-ups reparameterise ("CODA: the treasure hidden in the epilogue"):

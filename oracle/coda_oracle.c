@@ -6,7 +6,7 @@
  * block as the CODA write-ups describe it, so a reader can check it by eye.
  * It shares no code, header or constant with the CUDA library and must only
  * be called from the tests, the package smoke check and the benchmark's CPU
- * baseline leg.
+ * baseline leg and reference arm.
  *
  * Sources (the CODA news write-ups, three translations of one article):
  *   - "CODA: the treasure hidden in the epilogue": the GEMM -> residual add ->
