@@ -22,8 +22,10 @@ steps in the order the block applies them.
 
 Parity pins (tests/test_oracle.py): hand-derived 4x4 cases and a one-row chain
 in tests/golden/, numpy fp64 matmul on a C0-sized case, the reparameterisation
-identity, RMSNorm scale invariance, silu special values, and the E4M3 codec
-against torch's float8_e4m3fn over all 256 codes.
+identity, RMSNorm scale invariance, silu special values, the E4M3 codec
+against torch's float8_e4m3fn over all 256 codes, a hand-derived FP8 chain in
+which every quantisation site (and the fold before it) changes the result,
+and central finite differences for the backward functions.
 
 Weights are passed in the mathematical orientation W [K, N] (``nn.Linear``'s
 weight transposed).

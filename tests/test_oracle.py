@@ -44,6 +44,60 @@ def test_golden_full_chain():
             _close(out[k], c[k], 1e-12)
 
 
+def _fp8_case():
+    c = next(c for c in GOLDEN["cases"] if c["kind"] == "full_fp8")
+    return c, [A(c[k]) for k in ("X", "Wo", "R", "gamma1", "Wg", "Wu", "Wd", "gamma2", "Wq")]
+
+
+def test_golden_fp8_quantisation_sites():
+    """The quantisation-aware chain against a hand-derived case in which every
+    tensor holds values whose E4M3 rounding shows: X, Wo, the folded Wg, Wu,
+    Wq, Wd, h1, act and h2 are quantised (gamma folded first), R and r are not."""
+    c, args = _fp8_case()
+    out = oracle.chain_full_fp8(*args, c["eps"])
+    for k in ("h1", "r1", "act", "h2", "r2", "Z"):
+        _close(out[k], c[k], 1e-12)
+    # the case is sensitive to quantisation: the exact chain differs visibly
+    exact = oracle.chain_full(*args, c["eps"])
+    assert max(oracle.rel_err(exact[k], c[k]) for k in ("h1", "act", "h2", "Z")) > 1e-3
+
+
+def _fp8_chain_variant(args, eps, skip=(), fold_after=False, quant_R=False, r_from_q=False, resid_q=False):
+    """The FP8 chain composed from the oracle's steps with one site moved, to
+    show that the golden case above tells each misplacement apart."""
+    X, Wo, R, g1, Wg, Wu, Wd, g2, Wq = args
+    q = lambda n, t: t if n in skip else oracle.fake_quant_e4m3(t)[0]  # noqa: E731
+    if fold_after:
+        Wg_f, Wu_f, Wq_f = g1[:, None] * q("Wg", Wg), g1[:, None] * q("Wu", Wu), g2[:, None] * q("Wq", Wq)
+    else:
+        Wg_f, Wu_f, Wq_f = q("Wg", g1[:, None] * Wg), q("Wu", g1[:, None] * Wu), q("Wq", g2[:, None] * Wq)
+    h1 = oracle.gemm(q("X", X), q("Wo", Wo), oracle.fake_quant_e4m3(R)[0] if quant_R else R)
+    h1q = q("h1", h1)
+    _, r1 = oracle.rmsnorm(h1q if r_from_q else h1, g1, eps)
+    act = oracle.silu_mul(oracle.gemm(h1q, Wg_f) * r1[:, None], oracle.gemm(h1q, Wu_f) * r1[:, None])
+    h2 = oracle.gemm(q("act", act), q("Wd", Wd), h1q if resid_q else h1)
+    h2q = q("h2", h2)
+    _, r2 = oracle.rmsnorm(h2q if r_from_q else h2, g2, eps)
+    return {"h1": h1, "r1": r1, "act": act, "h2": h2, "r2": r2, "Z": oracle.gemm(h2q, Wq_f) * r2[:, None]}
+
+
+@pytest.mark.parametrize("mistake", [
+    {"skip": ("X",)}, {"skip": ("Wo",)}, {"skip": ("Wg",)}, {"skip": ("Wu",)}, {"skip": ("Wd",)}, {"skip": ("Wq",)},
+    {"skip": ("h1",)}, {"skip": ("act",)}, {"skip": ("h2",)}, {"fold_after": True}, {"quant_R": True},
+    {"r_from_q": True}, {"resid_q": True}], ids=lambda m: "-".join(f"{k}={v}" for k, v in m.items()))
+def test_fp8_golden_catches_each_misplaced_quantisation(mistake):
+    """A mistake planted in the composition (a quantisation dropped, the fold
+    after the quantisation, R quantised, r taken from the quantised h, the
+    quantised h1 as the down projection's residual) changes some output of
+    the golden case by far more than the 1e-12 its pin allows."""
+    c, args = _fp8_case()
+    right = _fp8_chain_variant(args, c["eps"])
+    for k in ("h1", "r1", "act", "h2", "r2", "Z"):
+        _close(right[k], c[k], 1e-12)
+    wrong = _fp8_chain_variant(args, c["eps"], **mistake)
+    assert max(oracle.rel_err(wrong[k], c[k]) for k in right) > 1e-4
+
+
 def test_golden_swiglu_gate_vs_up():
     c = GOLDEN["swiglu_gate_up"]
     _close(oracle.swiglu(A(c["Y"]), A(c["Wg"]), A(c["Wu"])), c["act"])
