@@ -1,40 +1,44 @@
-"""Benchmark of the fused GEMM-epilogue block on GB300.
+"""Benchmark of the fused GEMM-epilogue chain on GB300.
 
-Default workload: the LLaMA-3-1B attention-out block, bf16 in / fp32
-accumulate, M = 8192 tokens (batch 4 x seq 2048):
-    h = R + X Wo            X [8192, 2048], Wo [2048, 2048]   residual + partial RMS program
-    r = rms(h)                                                 reduction, in the consumer's epilogue
-    act = SwiGLU(r h Wg', r h Wu')   Wg, Wu [2048, 8192]       SwiGLU program
-One step = one pass of that chain over one batch.  The default
-``--reduce block`` runs it as one two-phase launch (coda_block_swiglu);
-``--reduce fused`` as 2 launches (coda_gemm_residual_partial_rms, then
-coda_gemm_swiglu_fused_rms); ``--reduce separate`` as 3 (coda_rms_reduce
-between them).  ``--workload`` selects the other configurations and
-``--pass backward|aux`` the backward chain or the memory-bound kernels.
+Default workload: the LLaMA-3-8B block tail, bf16 in / fp32 accumulate,
+M = 16384 tokens (batch 8 x seq 2048), hidden 4096, intermediate 14336:
+    h1 = R + X Wo                 X [16384, 4096], Wo [4096, 4096]   residual + partial RMS program
+    act = SwiGLU(r1 h1 Wg', r1 h1 Wu')   Wg, Wu [4096, 14336]         SwiGLU program, r1 reduced in its epilogue
+    h2 = h1 + act Wd              Wd [14336, 4096]                    residual + partial RMS program
+    Z = r2 h2 Wq'                 Wq [4096, 6144]                     row-scale program (next layer's QKV)
+7146.8 GFLOP per step.  One step = one pass of that chain over one batch.
+The default ``--reduce block`` runs it as two two-phase launches
+(coda_block_swiglu, then coda_block_rowscale); ``--reduce fused`` as 4
+launches (each reduction in its consumer's epilogue); ``--reduce separate``
+as 6 (coda_rms_reduce launches).  ``--workload`` selects the other
+configurations and ``--pass backward|aux`` the backward chain or the
+memory-bound kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl coda|reference|unfused]
 
 Prints ONE JSON line (rank 0).  ``value`` is the whole-job TFLOP/s with
-inputs resident in HBM (3 rotating sets of X, R and the weights, 143 MB
-each for the default workload, so every step reads inputs that are not in
-the 129 MB L2); ``e2e`` is the same metric with X and R copied in from
-pinned host memory and h and act copied back every step (copies of one step
-overlapped with the compute of its neighbours); ``roofline`` is the
-dominant kernel (the block kernel by default; the SwiGLU GEMM, 89% of the
-flops, with ``--reduce fused``) timed live with CUDA events around each of
-its launches; ``cpu_baseline`` is the fp64 CPU oracle timed on this host on
-a bounded row sample.  Multi-GPU: one process per GPU (torchrun), each rank
-runs its own independent batch (weak scaling, no collective on the data
-path; a barrier and a max-reduce of the elapsed time bracket the timed
-region).  ``--impl reference`` times the CPU oracle alone; ``--impl
-unfused`` times the unfused PyTorch sequence (cuBLAS GEMM, add, RMSNorm,
-GEMM, silu*mul), ``--compile`` the same under torch.compile.
+inputs resident in HBM (3 rotating sets of X, R and the weights, each larger
+than the 129 MB L2, so every step reads inputs that are not in L2); ``e2e``
+is the same metric with X and R copied in from pinned host memory and the
+chain's outputs copied back every step (copies of one step overlapped with
+the compute of its neighbours); ``roofline`` is the dominant kernel (the
+first block kernel by default) timed live with CUDA events around each of
+its launches; ``sustained`` repeats the step for a window of seconds, with
+the clocks sampled inside that window, so the figure holds under the power
+cap; ``cpu_baseline`` is the fp64 CPU oracle timed on this host on a bounded
+row sample.  Multi-GPU: one process per GPU (torchrun), each rank runs its
+own independent batch (weak scaling, no collective on the data path; a
+barrier and a max-reduce of the elapsed time bracket the timed region).
+``--impl reference`` times the CPU oracle alone; ``--impl unfused`` times the
+unfused PyTorch sequence (cuBLAS GEMM, add, RMSNorm, GEMM, silu*mul),
+``--compile`` the same under torch.compile.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -81,6 +85,32 @@ def algorithmic_bytes(M, K1, N, I, T):
     return fused, unfused
 
 
+def timed_kernel_bytes(w, mode, T):
+    """Compulsory HBM bytes of one launch of the kernel the roofline reports:
+    every operand, residual, output, partial and row scale read or written
+    once (weights once per launch).  Operands are 1 byte for e4m3 and 2 for
+    bf16; R, h and the outputs are bf16; P and r are fp32."""
+    a = 1 if w.dtype == "e4m3" else 2
+    o = 2
+    M = w.M
+
+    def residual(K, N):  # A [M, K], W [N, K], R [M, N] -> h [M, N], P [M, T]
+        return M * K * a + N * K * a + 2 * M * N * o + 4 * M * T
+
+    def consumer(N, N_out, n_weights):  # h [M, N], weights [N_out, N] -> out [M, N_out]; P -> r
+        red = 4 * M * T + 4 * M if mode != "separate" else 4 * M
+        return M * N * a + n_weights * N_out * N * a + M * N_out * o + red
+
+    if w.chain == "swiglu":
+        sw = consumer(w.N, w.N2, 2)
+        return residual(w.K1, w.N) + sw if mode == "block" else sw
+    if w.chain == "rowscale":
+        res = residual(w.K1, w.N)
+        return res + consumer(w.N, w.N2, 1) if mode == "block" else res
+    sw = consumer(w.N, w.inter, 2)
+    return residual(w.K1, w.N) + sw if mode == "block" else sw
+
+
 # Sources each kernel family is compiled from: a recorded ncu figure is valid
 # while the hash of its family's files is unchanged.
 KERNEL_SOURCES = {
@@ -110,15 +140,24 @@ def kernel_source_sha(family="gemm"):
 def recorded_traffic(kernel_tag):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", f"ncu_{kernel_tag}.md")
+    return recorded_traffic_with_source(kernel_tag)[0]
+
+
+def recorded_traffic_with_source(kernel_tag):
+    """(bytes per launch or None, where the figure comes from)."""
+    rel = os.path.join("profiles", f"ncu_{kernel_tag}.md")
+    p = os.path.join(ROOT, rel)
     if not os.path.exists(p):
-        return None
+        return None, f"no ncu summary {rel}"
     text = open(p).read()
     m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_sha and m_b) or m_sha.group(1) != kernel_source_sha():
-        return None
-    return float(m_b.group(1))
+    if not (m_sha and m_b):
+        return None, f"{rel} records no source_sha / dram_bytes_per_launch"
+    if m_sha.group(1) != kernel_source_sha():
+        return None, f"{rel} was taken on other kernel sources ({m_sha.group(1)}, now {kernel_source_sha()})"
+    return float(m_b.group(1)), (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, committed in "
+                                 f"{rel} (kernel sources {m_sha.group(1)}), not measured in this run")
 
 
 class ClockSampler:
@@ -186,6 +225,23 @@ class ClockSampler:
         reasons = sorted({names[i] for r in loaded for i in range(4) if r[4 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(loaded[0][1]),
                 "power_w_max": pmax, "samples": len(loaded), "reasons": reasons}
+
+
+def max_over_ranks(x, dist, dev):
+    """The largest of every rank's x (the job ends when its slowest rank
+    does); x itself when there is one rank."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step, steps, world_size, seconds):
+    """Whole-job throughput: every rank runs its own batches (weak scaling),
+    so the job does world_size x steps x flops_per_step in the slowest rank's
+    time."""
+    return flops_per_step * steps * world_size / seconds / 1e12
 
 
 def dist_setup(backend):
@@ -289,7 +345,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, "separate"),
+        "config": config_of(w),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "cpu": cpu_model(),
                          "sample": f"{rows} rows of the {w.M}-row batch per step (rows are independent), "
                                    f"fp64 unfused oracle"},
@@ -336,8 +392,10 @@ def set_bytes(w):
     return x + wts
 
 
-def config_of(w, reduce="separate"):
-    return {"workload": w.name, "chain": chain_description(w, reduce), "dtype": w.dtype,
+def config_of(w):
+    """The workload alone (shapes, dtype, seed, L2 policy): identical for every
+    arm that runs it, whatever launches that arm uses."""
+    return {"workload": w.name, "dtype": w.dtype,
             "M": w.M, "hidden": w.N, "K1": w.K1, "out_or_intermediate": w.inter or w.N2, "N2": w.N2,
             "eps": w.eps, "seed": w.seed, "heavy_rows": w.heavy_rows,
             "l2": f"{NSETS} rotating input sets of {set_bytes(w) / 1e6:.0f} MB each (> 129 MB L2); no flush"}
@@ -487,7 +545,7 @@ def make_step(g, C, w, mode, eps, ws=None):
                                          scale_w=q8["Wdt"][1], amax_h=st["a3"])
         g.coda_quantize_e4m3(st["h2"], st["a3"], st["h2q"], st["s3"])
         rs(st["h2q"], q8["Wqt"][0], st["P2"], st["r2"], st["Z"], scale_h=st["s3"], scale_w=q8["Wqt"][1])
-    return step, (8 if fused else 10)
+    return step, (9 if fused else 11)
 
 
 def run_coda(args, w):
@@ -542,12 +600,31 @@ def run_coda(args, w):
     elapsed = t_start.elapsed_time(t_end) / 1e3
     dom_ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
     g.coda_get_device_status()
-    elapsed_max = elapsed
-    if dist is not None:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_max = float(t.item())
-    value = step_flops * args.steps * ws / elapsed_max / 1e12
+    elapsed_max = max_over_ranks(elapsed, dist, dev)
+    value = job_tflops(step_flops, args.steps, ws, elapsed_max)
+
+    # ---- sustained: the same step repeated for a window of seconds, so the
+    # clocks sampled inside it describe the kernel under the power cap (a
+    # short timed region runs at burst clocks before the cap engages)
+    sustained = None
+    if args.sustained_s > 0:
+        n_sus = max(args.steps, math.ceil(args.sustained_s / max(elapsed / args.steps, 1e-6)))
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_sus)]
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk_s:
+            barrier()
+            s0.record(stream)
+            for i in range(n_sus):
+                step(sets[i % NSETS], sev[i])
+            s1.record(stream)
+            barrier()
+        sus_s = s0.elapsed_time(s1) / 1e3
+        sus_dom_ms = statistics.fmean(a.elapsed_time(b) for a, b in sev)
+        g.coda_get_device_status()
+        sus_s = max_over_ranks(sus_s, dist, dev)
+        sustained = {"steps": n_sus, "seconds": sus_s, "value": job_tflops(step_flops, n_sus, ws, sus_s),
+                     "ms_per_step": sus_s / n_sus * 1e3, "kernel_avg_launch_ms": sus_dom_ms,
+                     "clocks": clk_s.summary()}
 
     # ---- end to end: pinned host X, R in and the block's outputs out, every
     # step.  Two buffer slots and three streams, so one step's copies overlap
@@ -594,12 +671,8 @@ def run_coda(args, w):
         e2e_step(i)
     e1.record(s_out)  # after every step's last copy (s_out runs the steps' copies in order)
     barrier()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_val = step_flops * e2e_steps * ws / e2e_s / 1e12
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, dev)
+    e2e_val = job_tflops(step_flops, e2e_steps, ws, e2e_s)
     sl = slots[0]
     h2d = sum(sl[k].numel() * sl[k].element_size() for k in ("hX", "hR"))
     d2h = sum(sl["h_" + o].numel() * sl["h_" + o].element_size() for o in outs)
@@ -610,16 +683,20 @@ def run_coda(args, w):
     ratio, dtname = (2.0, "e4m3 (2 x measured bf16 burst, the nominal fp8/bf16 ratio)") if w.dtype == "e4m3" else \
         (1.0, "bf16 burst")
     peak = pk["bf16_tflops"] * ratio
+    peak_sus = pk["bf16_tflops_sustained"] * ratio
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    tag = f"{dom.split(' ')[0]}_{w.name}"
+    traffic, traffic_src = recorded_traffic_with_source(tag)
     roof = {"kernel": f"{dom} (tcgen05, {w.dtype})", "bound": "tensor", "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": f"{dtname}, {pk_kind}",
-            "frac_of_sustained": achieved / (pk["bf16_tflops_sustained"] * ratio),
-            "traffic": recorded_traffic(f"{dom.split(' ')[0]}_{w.name}"), "avg_launch_ms": dom_ms}
+            "traffic": traffic, "traffic_source": traffic_src, "avg_launch_ms": dom_ms,
+            "flops_per_launch": dom_flops,
+            "algorithmic_bytes": timed_kernel_bytes(w, mode, g.coda_partial_cols(w.N))}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if w.dtype == "e4m3" else "bf16",
-        "data": "synthetic", "config": config_of(w, args.reduce),
+        "data": "synthetic", "config": config_of(w), "chain": chain_description(w, mode),
         "frac_of_peak": value / ws / peak,
         "roofline": roof,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -628,12 +705,17 @@ def run_coda(args, w):
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
     }
+    if sustained is not None:
+        sus_kernel = dom_flops / (sustained["kernel_avg_launch_ms"] / 1e3) / 1e12
+        clk_s = sustained.pop("clocks")
+        sustained.update({"frac_of_bf16_sustained": sustained["value"] / ws / peak_sus,
+                          "kernel_achieved": sus_kernel, "kernel_frac_of_bf16_sustained": sus_kernel / peak_sus,
+                          "peak_sustained": peak_sus, "sm_mhz_median_under_load": clk_s.get("sm_mhz"),
+                          "clocks": clk_s})
+        line["sustained"] = sustained
     if w.chain == "swiglu":
         fused_b, unfused_b = algorithmic_bytes(w.M, w.K1, w.N, w.N2, g.coda_partial_cols(w.N))
         line["dram_bytes_algorithmic"] = {"fused": sum(fused_b.values()), "unfused": unfused_b}
-        # the timed kernel's compulsory bytes: the SwiGLU GEMM alone, or in block
-        # mode both programs of the one launch (h written, then read back)
-        roof["algorithmic_bytes"] = fused_b["swiglu"] + (fused_b["gemm_residual"] if mode == "block" else 0)
     if not args.no_cpu_baseline:
         n, dt, fl_cpu, threads = oracle_sample(w, inp, args.cpu_budget)
         line["cpu_baseline"] = {"value": fl_cpu / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -727,7 +809,7 @@ def run_coda_backward(args, w):
     print(json.dumps({
         "metric": METRIC, "pass": "backward", "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["backward"] * 1e3, "higher_is_better": True, "scaling": "weak",
-        "dtype": "bf16", "data": "synthetic", "config": config_of(w, "fused"),
+        "dtype": "bf16", "data": "synthetic", "config": config_of(w),
         "frac_of_peak": value / ws / pk["bf16_tflops"],
         "train_forward_with_saves": {"value": sum(gemm_flops_by_kernel(w).values()) / res["train_forward"] / 1e12,
                                      "ms_per_step": res["train_forward"] * 1e3},
@@ -795,7 +877,7 @@ def run_unfused_backward(args, w):
     print(json.dumps({"impl": "unfused_torch_compile_autograd" if args.compile else "unfused_torch_eager_autograd",
                       "pass": "backward", "metric": METRIC,
                       "value": backward_flops(w) / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
-                      "steps": args.steps, "dtype": "bf16", "config": config_of(w, "separate")}), flush=True)
+                      "steps": args.steps, "dtype": "bf16", "config": config_of(w)}), flush=True)
 
 
 def run_unfused(args, w):
@@ -840,7 +922,7 @@ def run_unfused(args, w):
     if rank == 0:
         print(json.dumps({"impl": "unfused_torch_compile" if args.compile else "unfused_torch_eager", "metric": METRIC, "value": fl * args.steps / dt / 1e12,
                           "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-                          "ms_per_step": dt / args.steps * 1e3, "dtype": "bf16", "config": config_of(w, "separate")}),
+                          "ms_per_step": dt / args.steps * 1e3, "dtype": "bf16", "config": config_of(w)}),
               flush=True)
 
 
@@ -930,10 +1012,10 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["coda", "reference", "unfused"], default="coda")
-    ap.add_argument("--workload", default="llama1b_attn_out_swiglu",
+    ap.add_argument("--workload", default="llama8b_chain",
                     choices=["llama1b_attn_out_swiglu", "llama1b_mlp_down_qkv", "llama8b_chain", "llama8b_chain_fp8"],
-                    help="the default is the configuration the metric is quoted on; the others are for the "
-                         "per-configuration tables")
+                    help="the default is the largest bf16 configuration (the LLaMA-3-8B chain); the others "
+                         "are for the per-configuration tables")
     ap.add_argument("--reduce", choices=["block", "fused", "separate"], default="block",
                     help="block: residual GEMM and consumer in one persistent launch per block; fused: r reduced "
                          "inside the consumer GEMM's epilogue; separate: coda_rms_reduce launch")
@@ -948,6 +1030,8 @@ def main():
                     help="with --profile-step: override the workload's M (tokens), for ncu captures on a smaller "
                          "case of the same kernels")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--sustained-s", type=float, default=2.0,
+                    help="seconds of the sustained window after the timed steps (0: none)")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="--impl reference: seconds of oracle work for warm-up + timed steps together")
     args = ap.parse_args()

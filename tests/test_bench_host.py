@@ -47,3 +47,37 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     (csrc / "k.cuh").write_text("header v2")
     assert bench.recorded_traffic("x") is None
     assert bench.recorded_traffic("missing") is None
+
+
+def test_timed_kernel_bytes_of_the_block_launches():
+    from coda_inputs import WORKLOADS
+    # LLaMA-3-1B attention-out block in one launch: X, Wo, R, h, P, then h, Wg, Wu, act, P, r
+    assert bench.timed_kernel_bytes(WORKLOADS["llama1b_attn_out_swiglu"], "block", 16) / 1e6 == \
+        pytest.approx(345.0, abs=1.0)
+    # LLaMA-3-8B chain, first block (Wo + gate/up): 438.3 MB of phase A, 841.0 MB of phase B
+    w = WORKLOADS["llama8b_chain"]
+    M, H, I, T = w.M, w.N, w.inter, 32
+    phase_a = 2 * (M * H + H * H + 2 * M * H) + 4 * M * T
+    phase_b = 2 * (M * H + 2 * I * H + M * I) + 4 * M * T + 4 * M
+    assert bench.timed_kernel_bytes(w, "block", T) == phase_a + phase_b
+    assert bench.timed_kernel_bytes(w, "fused", T) == phase_b
+    assert (phase_a + phase_b) / 1e6 == pytest.approx(1279.3, abs=0.5)
+
+
+def test_config_names_the_workload_only():
+    """Both arms print config_of(w): it holds the workload's keys, none that
+    depend on how an arm runs it, so the two arms' configs are identical."""
+    from coda_inputs import WORKLOADS
+    for w in WORKLOADS.values():
+        c = bench.config_of(w)
+        assert c["workload"] == w.name and c["M"] == w.M and c["dtype"] == w.dtype
+        assert "chain" not in c and not any("launch" in str(v) for v in c.values())
+
+
+def test_default_workload_is_the_8b_chain(monkeypatch):
+    seen = {}
+    monkeypatch.setattr(bench, "run_coda", lambda args, w: seen.update(w=w, args=args))
+    monkeypatch.setattr("sys.argv", ["bench.py"])
+    bench.main()
+    assert seen["w"].name == "llama8b_chain" and seen["args"].reduce == "block"
+    assert seen["args"].sustained_s >= 2.0
