@@ -196,14 +196,19 @@ CUresult encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 }
 
 cudaError_t launch_ex(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                      void** args, int cluster) {
+                      void** args, int cluster, bool cooperative) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int n = 0;
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
   if (pdl) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
@@ -715,11 +720,15 @@ int64_t coda_block_workspace_bytes(int64_t M) {
 namespace {
 
 // Shared by the one-launch blocks: residual GEMM (phase A) and its consumer
-// (phase B) with the reduction folded into the consumer's epilogue.
-coda_status block_impl(int epi_b, const void* X, const void* W1t, const void* R, const void* Wb, const void* Wb2,
-                       float eps, void* H, float* P, float* r_out, void* Out, int64_t M, int64_t N, int64_t K,
-                       int64_t N_out, coda_dtype dtype, void* workspace, cudaStream_t stream) {
+// (phase B) with the reduction folded into the consumer's epilogue.  Checks
+// every argument and fills *p; enqueues nothing.  M == 0 leaves p->M at 0
+// (nothing to launch).
+coda_status block_prepare(int epi_b, const void* X, const void* W1t, const void* R, const void* Wb, const void* Wb2,
+                          float eps, void* H, float* P, float* r_out, void* Out, int64_t M, int64_t N, int64_t K,
+                          int64_t N_out, coda_dtype dtype, void* workspace, cudaStream_t stream,
+                          coda::GemmProblem* pp) {
   g_msg[0] = 0;
+  *pp = coda::GemmProblem{};
   if (dtype == CODA_E4M3)
     return fail(CODA_ERR_UNSUPPORTED,
                 "one-launch blocks take CODA_F32 or CODA_BF16: FP8 needs the per-tensor amax of h before its consumer");
@@ -745,7 +754,7 @@ coda_status block_impl(int epi_b, const void* X, const void* W1t, const void* R,
   const Range ins[] = {rng("X", X, M * K * ib), rng("W1t", W1t, N * K * ib), rng("R", R, M * N * ob),
                        rng("W", Wb, N_out * N * ib), rng("Wut", Wb2, Wb2 ? N_out * N * ib : 0)};
   TRY(check_overlaps(outs, 5, ins, 5));
-  coda::GemmProblem p = {};
+  coda::GemmProblem& p = *pp;
   p.epi = coda::kEpiResidualPartialRms;
   p.A = X;
   p.B = W1t;
@@ -771,6 +780,15 @@ coda_status block_impl(int epi_b, const void* X, const void* W1t, const void* R,
   p.band_ready = static_cast<unsigned*>(workspace);
   p.stream = stream;
   p.pdl = use_pdl();
+  return CODA_OK;
+}
+
+coda_status block_impl(int epi_b, const void* X, const void* W1t, const void* R, const void* Wb, const void* Wb2,
+                       float eps, void* H, float* P, float* r_out, void* Out, int64_t M, int64_t N, int64_t K,
+                       int64_t N_out, coda_dtype dtype, void* workspace, cudaStream_t stream) {
+  coda::GemmProblem p;
+  TRY(block_prepare(epi_b, X, W1t, R, Wb, Wb2, eps, H, P, r_out, Out, M, N, K, N_out, dtype, workspace, stream, &p));
+  if (p.M == 0) return CODA_OK;
   return run_gemm(dtype, p);
 }
 
@@ -893,9 +911,14 @@ extern "C" coda_status coda_block_swiglu_noalloc(const void* X, const void* W1t,
   if (M <= 0) return coda_block_swiglu(X, W1t, R, Wgt, Wut, eps, H, P, r_out, Act, M, N, K, I, dtype, nullptr, stream);
   void* counters = nullptr;
   TRY(noalloc_counters(&counters));
+  // every argument is checked before anything is enqueued, so a rejected
+  // call leaves the shared array untouched
+  coda::GemmProblem p;
+  TRY(block_prepare(coda::kEpiSwiGLU, X, W1t, R, Wgt, Wut, eps, H, P, r_out, Act, M, N, K, I, dtype, counters, stream,
+                    &p));
   // every call shares the array: start from zero whatever the last call left
   const int64_t bytes = coda_block_workspace_bytes(M);
   cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(bytes), stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(band counters)");
-  return coda_block_swiglu(X, W1t, R, Wgt, Wut, eps, H, P, r_out, Act, M, N, K, I, dtype, counters, stream);
+  return run_gemm(dtype, p);
 }

@@ -133,8 +133,43 @@ CUresult encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 // Launch `kernel` with the given shape, optionally with programmatic stream
 // serialisation (PDL), so its prologue overlaps the previous kernel's tail,
-// and in clusters of `cluster` CTAs along x.
+// in clusters of `cluster` CTAs along x, and as a cooperative launch (every
+// CTA of the grid resident at once, or the launch fails).
 cudaError_t launch_ex(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                      void** args, int cluster = 1);
+                      void** args, int cluster = 1, bool cooperative = false);
+
+// A two-phase launch (band waits between CTAs) first asks for a cooperative
+// launch, which makes the co-residency of its grid a guarantee.  What to do
+// with that attempt's result:
+//   kCoopDone      launched
+//   kCoopFallback  the runtime or device does not take a cooperative launch
+//                  of this form (with clusters): launch it plainly, on a
+//                  grid no larger than the co-resident CTAs of an idle GPU
+//   kCoopError     any other error, cudaErrorCooperativeLaunchTooLarge
+//                  included: report it, never launch a grid that might not
+//                  fit
+enum CoopAction { kCoopDone = 0, kCoopFallback = 1, kCoopError = 2 };
+inline CoopAction cooperative_action(cudaError_t e) {
+  if (e == cudaSuccess) return kCoopDone;
+  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration)
+    return kCoopFallback;
+  return kCoopError;
+}
+
+// One launch of a grid whose CTAs wait on each other: `launch(cooperative)`
+// issues one attempt.  With try_coop, the cooperative form goes first and
+// the plain form follows only on kCoopFallback (*refused is then set, so the
+// caller can skip the attempt on that device from then on).
+template <class F>
+cudaError_t launch_coresident(F&& launch, bool try_coop, bool* refused) {
+  *refused = false;
+  if (try_coop) {
+    const cudaError_t e = launch(true);
+    if (cooperative_action(e) != kCoopFallback) return e;
+    (void)cudaGetLastError();  // a refused launch configuration is not sticky: clear it
+    *refused = true;
+  }
+  return launch(false);
+}
 
 }  // namespace coda

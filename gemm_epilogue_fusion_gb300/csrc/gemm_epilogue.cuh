@@ -56,6 +56,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cstdlib>
+#include <mutex>
 #include <type_traits>
 
 #include "coda_internal.h"
@@ -965,45 +966,61 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
     return cudaErrorInvalidValue;
   }
   auto kernel = gemm_epilogue_kernel<C>;
-  // per device: shared-memory opt-in and the number of co-resident CTA pairs
+  // per device: shared-memory opt-in, the number of co-resident units, and
+  // (two-phase) whether the device takes a cooperative launch of this form;
+  // two host threads may make their first launch at once
+  static std::mutex mu;
   static int configured_mask = 0;
   static int max_units[32] = {0};
+  static int coop_plain_mask = 0;  // devices that refused the cooperative form
   int dev = 0;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return ce;
-  if (dev >= 32 || !(configured_mask & (1 << dev))) {
-    ce = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (ce != cudaSuccess) {
-      *msg = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
-      return ce;
-    }
-    int units = device_sm_count();
-    if (C::CG == 2) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * units);
-      cfg.blockDim = dim3(C::NUM_THREADS);
-      cfg.dynamicSmemBytes = C::SMEM_BYTES;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int clusters = 0;
-      ce = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(kernel), &cfg);
-      if (ce != cudaSuccess || clusters <= 0) {
-        *msg = "cudaOccupancyMaxActiveClusters failed for the CTA-pair GEMM";
-        return ce != cudaSuccess ? ce : cudaErrorInvalidConfiguration;
+  int units = 0;
+  // CODA_NO_COOPERATIVE=1 launches two-phase grids plainly: for profilers that
+  // cannot replay a cooperative clustered launch (the co-residency contract
+  // then rests on the caller, as on a device that refuses the cooperative form)
+  static const bool no_coop = getenv("CODA_NO_COOPERATIVE") != nullptr;
+  bool cooperative = C::TWO_PHASE && !no_coop;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 32 || !(configured_mask & (1 << dev))) {
+      ce = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      if (ce != cudaSuccess) {
+        *msg = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
+        return ce;
       }
-      units = clusters;
+      int u = device_sm_count();
+      if (C::CG == 2) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * u);
+        cfg.blockDim = dim3(C::NUM_THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        ce = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(kernel), &cfg);
+        if (ce != cudaSuccess || clusters <= 0) {
+          *msg = "cudaOccupancyMaxActiveClusters failed for the CTA-pair GEMM";
+          return ce != cudaSuccess ? ce : cudaErrorInvalidConfiguration;
+        }
+        u = clusters;
+      }
+      if (dev < 32) {
+        max_units[dev] = u;
+        configured_mask |= 1 << dev;
+      }
+      units = u;
+    } else {
+      units = max_units[dev];
     }
-    if (dev < 32) {
-      max_units[dev] = units;
-      configured_mask |= 1 << dev;
-    }
+    if (dev < 32 && (coop_plain_mask & (1 << dev))) cooperative = false;
   }
-  const int units = dev < 32 ? max_units[dev] : device_sm_count() / C::CG;
   const int m_tiles = (p.M + C::TILE_M - 1) / C::TILE_M;
   int num_tiles = m_tiles * ((p.N_out + C::out_cols(C::kEpiA) - 1) / C::out_cols(C::kEpiA));
   if constexpr (C::TWO_PHASE) num_tiles += m_tiles * ((p.b.N_out + C::out_cols(C::kEpiB) - 1) / C::out_cols(C::kEpiB));
@@ -1017,8 +1034,19 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
   PhaseArgs pb = {p.b.N_out, p.b.K, p.b.ep, group_b};
   unsigned* band_ready = p.band_ready;
   void* args[] = {&tmA, &tmB, &tmB2, &tmR, &tmD, &tmA_b, &tmB_b, &tmB2_b, &tmD_b, &M, &pa, &pb, &band_ready};
-  ce = launch_ex(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(C::NUM_THREADS), C::SMEM_BYTES, p.stream,
-                 p.pdl, args, C::CG);
+  bool refused = false;
+  ce = launch_coresident(
+      [&](bool coop) {
+        return launch_ex(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(C::NUM_THREADS), C::SMEM_BYTES,
+                         p.stream, p.pdl, args, C::CG, coop);
+      },
+      cooperative, &refused);
+  if (refused && dev < 32) {
+    // this device takes no cooperative launch of a clustered grid: the grid
+    // stays sized to the co-resident units of an idle GPU
+    std::lock_guard<std::mutex> lock(mu);
+    coop_plain_mask |= 1 << dev;
+  }
   if (ce != cudaSuccess) *msg = "GEMM kernel launch failed";
   return ce;
 }

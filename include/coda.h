@@ -230,9 +230,19 @@ CODA_API coda_status coda_gemm_swiglu_fused_rms(const void* H, const void* Wgt, 
  *     by the caller before its first use; every call leaves it zeroed again
  *     (the last CTA to finish resets it), so it can be reused without a
  *     memset.  Calls that share a workspace must not overlap on the GPU.
- *   The grid never exceeds the CTAs that fit on the GPU at once, which the
- *   band waits require; each wait is bounded and reports CODA_ERR_TIMEOUT
- *   through coda_get_device_status(). */
+ *   Co-residency: the band waits need every CTA of the grid resident at
+ *   once.  The grid never exceeds the CTAs that fit on an idle GPU, and the
+ *   kernel is launched cooperatively, which makes the runtime either start
+ *   the whole grid together or fail the launch (CODA_ERR_CUDA).  If a device
+ *   or runtime refuses a cooperative launch of a clustered grid, the library
+ *   notes that once per device and launches plainly from then on (as it
+ *   does when the environment sets CODA_NO_COOPERATIVE, for profilers that
+ *   cannot replay a cooperative clustered launch); the co-residency then
+ *   rests on the caller: while such a launch runs, no
+ *   kernel on another stream may hold SMs that its CTAs need.  If that
+ *   contract is broken, a band wait runs out after 2 s and the call reports
+ *   CODA_ERR_TIMEOUT through coda_get_device_status(), with partial outputs;
+ *   it does not hang.  Every wait is bounded the same way. */
 CODA_API int64_t coda_block_workspace_bytes(int64_t M);
 CODA_API coda_status coda_block_rowscale(const void* X, const void* W1t, const void* R, const void* W2t, float eps,
                                          void* H, float* P, float* r_out, void* Z, int64_t M, int64_t N, int64_t K,
@@ -253,6 +263,10 @@ CODA_API coda_status coda_block_swiglu(const void* X, const void* W1t, const voi
  *   Limit: M <= 131072 rows; larger M returns CODA_ERR_INVALID_ARG.
  *   The first call on a device looks up the array's device address for that
  *   device (with it current); make that first call before any stream capture.
+ *   The address is kept for the life of the process: after cudaDeviceReset
+ *   on a device, do not call this entry point on that device again.
+ *   Arguments are checked before anything is enqueued: a rejected call
+ *   leaves the shared array as it was.
  *   Every call shares the one array: each call zeroes the counters it uses
  *   (an asynchronous memset on `stream`) before its kernel, so calls that
  *   overlap on the GPU, on any streams, race and must not be issued.

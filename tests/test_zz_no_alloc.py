@@ -41,9 +41,24 @@ def test_noalloc_block_matches_workspace_block_twice(w):
     d, Wg, Wu = _inputs(w)
     ws = g.block_workspace(w.M, "cuda")
     h_ref, P_ref, act_ref = g.coda_block_swiglu(d["X"], d["W1t"], d["R"], Wg, Wu, w.eps, ws)
-    for _ in range(2):
-        h, P, act = g.coda_block_swiglu_noalloc(d["X"], d["W1t"], d["R"], Wg, Wu, w.eps)
+    # the caller's outputs, allocated once up front: the calls themselves must allocate nothing
+    T = g.coda_partial_cols(w.N)
+    h = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
+    P = torch.empty(w.M, T, dtype=torch.float32, device="cuda")
+    act = torch.empty(w.M, w.N2, dtype=torch.bfloat16, device="cuda")
+    r = torch.empty(w.M, dtype=torch.float32, device="cuda")
+    for call in range(2):
         torch.cuda.synchronize()
+        allocs = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+        free = torch.cuda.mem_get_info()[0]
+        g.coda_block_swiglu_noalloc(d["X"], d["W1t"], d["R"], Wg, Wu, w.eps, H=h, P=P, Act=act, r_out=r)
+        torch.cuda.synchronize()
+        if call == 1:
+            # the first call may load the kernel's code onto the device; from
+            # then on a call changes neither torch's allocations nor the
+            # device's free memory
+            assert torch.cuda.memory_stats().get("allocation.all.allocated", 0) == allocs
+            assert torch.cuda.mem_get_info()[0] == free
         for got, ref in ((h, h_ref), (P, P_ref), (act, act_ref)):
             assert oracle.rel_err(got.cpu(), ref.cpu()) <= TOL
     g.coda_get_device_status()
