@@ -101,6 +101,11 @@ def timed_kernel_bytes(w, mode, T):
         red = 4 * M * T + 4 * M if mode != "separate" else 4 * M
         return M * N * a + n_weights * N_out * N * a + M * N_out * o + red
 
+    if w.dtype == "e4m3" and mode == "block":
+        # FP8 block 1: X read (bf16) and quantised (Xq written, then read by
+        # the GEMM), h1 read back and quantised (h1q written, then read)
+        quant = lambda rows, cols: rows * cols * (o + 2 * a)  # noqa: E731
+        return quant(M, w.K1) + residual(w.K1, w.N) + quant(M, w.N) + consumer(w.N, w.inter, 2)
     if w.chain == "swiglu":
         sw = consumer(w.N, w.N2, 2)
         return residual(w.K1, w.N) + sw if mode == "block" else sw
@@ -114,9 +119,9 @@ def timed_kernel_bytes(w, mode, T):
 # Sources each kernel family is compiled from: a recorded ncu figure is valid
 # while the hash of its family's files is unchanged.
 KERNEL_SOURCES = {
-    "gemm": ["coda_internal.h", "gemm_epilogue.cuh", "sm103_ptx.cuh", "coda_gemm_bf16.cu", "coda_gemm_tf32.cu",
-             "coda_gemm_e4m3.cu"],
-    "aux": ["coda_internal.h", "sm103_ptx.cuh", "coda_aux.cu"],
+    "gemm": ["coda_internal.h", "gemm_epilogue.cuh", "sm103_ptx.cuh", "fp8_e4m3.cuh", "coda_gemm_bf16.cu",
+             "coda_gemm_tf32.cu", "coda_gemm_e4m3.cu"],
+    "aux": ["coda_internal.h", "sm103_ptx.cuh", "fp8_e4m3.cuh", "coda_aux.cu"],
 }
 
 
@@ -363,7 +368,11 @@ E2E_OUT = {"swiglu": ("h", "act"), "rowscale": ("h", "Z"), "full": ("h2", "Z")}
 
 
 def chain_description(w, reduce):
-    if reduce == "block" and w.dtype != "e4m3":
+    if reduce == "block" and w.dtype == "e4m3":
+        return ("amax(X) -> coda_block_swiglu_fp8 (quantise X, Wo + residual + partial RMS + amax(h1), quantise h1, "
+                "gate/up SwiGLU with the reduction in its epilogue + amax(act), one persistent launch) -> "
+                "coda_block_rowscale_fp8 (quantise act, down + residual h1 + amax(h2), quantise h2, QKV)")
+    if reduce == "block":
         if w.chain == "full":
             return ("coda_block_swiglu (Wo + residual + partial RMS, then gate/up SwiGLU with the reduction in its "
                     "epilogue, one persistent launch) -> coda_block_rowscale (down + residual h1, then QKV)")
@@ -459,7 +468,7 @@ def prepare_set(g, C, w, inp, dev, rank, s):
     return st
 
 
-def make_step(g, C, w, mode, eps, ws=None):
+def make_step(g, C, w, mode, eps, ws=None, fp8_x="block", fp8_act="block"):
     """One pass of the workload's chain over a set; ``ev`` (a pair of CUDA
     events) brackets the dominant kernel's launch.  mode: "separate"
     (rms_reduce launch), "fused" (reduction in the consumer's epilogue) or
@@ -470,7 +479,34 @@ def make_step(g, C, w, mode, eps, ws=None):
         if ev is not None:
             ev[i].record(torch.cuda.current_stream())
 
-    if mode == "block" and w.dtype != "e4m3":
+    if mode == "block" and w.dtype == "e4m3":
+        # amax(X), then the two FP8 one-launch blocks: block 1 quantises X,
+        # runs Wo, quantises h1 and runs gate/up; block 2 quantises act, runs
+        # the down projection, quantises h2 and runs QKV
+        x_in_block = fp8_x == "block"
+        act_in_block = fp8_act == "block"
+
+        def step(st, ev=None):
+            q8 = st["q8"]
+            g.coda_amax(st["X"], st["ax"])
+            if not x_in_block:
+                g.coda_quantize_e4m3(st["X"], st["ax"], st["Xq"], st["sx"])
+            mark(ev, 0)
+            g.coda_block_swiglu_fp8(st["X"] if x_in_block else None, st["ax"] if x_in_block else None,
+                                    q8["Wot"][0], q8["Wot"][1], st["R"], q8["Wgt"][0],
+                                    q8["Wgt"][1], q8["Wut"][0], q8["Wut"][1], eps, ws, Aq=st["Xq"], scale_a=st["sx"],
+                                    H=st["h1"], P=st["P1"], r_out=st["r1"], amax_h=st["a1"], Hq=st["h1q"],
+                                    scale_h=st["s1"], Act=st["act"], amax_act=st["a2"])
+            mark(ev, 1)
+            if not act_in_block:
+                g.coda_quantize_e4m3(st["act"], st["a2"], st["actq"], st["s2"])
+            g.coda_block_rowscale_fp8(st["act"] if act_in_block else None, st["a2"] if act_in_block else None,
+                                      q8["Wdt"][0], q8["Wdt"][1], st["h1"], q8["Wqt"][0],
+                                      q8["Wqt"][1], eps, ws, Aq=st["actq"], scale_a=st["s2"], H=st["h2"], P=st["P2"],
+                                      r_out=st["r2"], amax_h=st["a3"], Hq=st["h2q"], scale_h=st["s3"], Z=st["Z"])
+        return step, 3 + (0 if x_in_block else 1) + (0 if act_in_block else 1)
+
+    if mode == "block":
         if w.chain == "swiglu":
             def step(st, ev=None):
                 mark(ev, 0)
@@ -560,16 +596,20 @@ def run_coda(args, w):
     inp = make_inputs(w)
     sets = [prepare_set(g, C, w, inp, dev, rank, s) for s in range(NSETS)]
     torch.cuda.synchronize()
-    mode = args.reduce if not (args.reduce == "block" and w.dtype == "e4m3") else "fused"
-    wksp = g.block_workspace(w.M, dev)
-    step, launches = make_step(g, C, w, mode, w.eps, wksp)
+    # FP8 defaults to the nine-launch chain: the FP8 blocks (one launch per
+    # block, quantisation in the launch) measured slower on GB300
+    mode = args.reduce if args.reduce != "auto" else ("fused" if w.dtype == "e4m3" else "block")
+    wksp = g.block_fp8_workspace(w.M, dev) if w.dtype == "e4m3" else g.block_workspace(w.M, dev)
+    step, launches = make_step(g, C, w, mode, w.eps, wksp, args.fp8_x, args.fp8_act)
     fl = gemm_flops_by_kernel(w)
     step_flops = sum(fl.values())
     dom = DOMINANT[w.chain]
     dom_flops = fl[dom]
     if mode == "block":  # the timed launch holds both GEMMs of the (first) block
         if w.chain == "full":
-            dom, dom_flops = "block_swiglu (Wo + gate/up)", fl["gemm_residual_partial_rms(Wo)"] + fl["gemm_swiglu"]
+            name = "block_swiglu_fp8 (quantise X, Wo, quantise h1, gate/up)" if w.dtype == "e4m3" else \
+                "block_swiglu (Wo + gate/up)"
+            dom, dom_flops = name, fl["gemm_residual_partial_rms(Wo)"] + fl["gemm_swiglu"]
         else:
             dom, dom_flops = f"block_{w.chain}", step_flops
     stream = torch.cuda.current_stream(dev)
@@ -1016,9 +1056,16 @@ def main():
                     choices=["llama1b_attn_out_swiglu", "llama1b_mlp_down_qkv", "llama8b_chain", "llama8b_chain_fp8"],
                     help="the default is the largest bf16 configuration (the LLaMA-3-8B chain); the others "
                          "are for the per-configuration tables")
-    ap.add_argument("--reduce", choices=["block", "fused", "separate"], default="block",
-                    help="block: residual GEMM and consumer in one persistent launch per block; fused: r reduced "
-                         "inside the consumer GEMM's epilogue; separate: coda_rms_reduce launch")
+    ap.add_argument("--reduce", choices=["auto", "block", "fused", "separate"], default="auto",
+                    help="block: residual GEMM and consumer in one persistent launch per block (FP8: the FP8 "
+                         "blocks, which also quantise h); fused: r reduced inside the consumer GEMM's epilogue; "
+                         "separate: coda_rms_reduce launch; auto: block for bf16, fused for FP8")
+    ap.add_argument("--fp8-x", choices=["block", "kernel"], default="block",
+                    help="FP8 block mode: X quantised by the first block's quantiser warps, or by "
+                         "coda_quantize_e4m3 before it")
+    ap.add_argument("--fp8-act", choices=["block", "kernel"], default="block",
+                    help="FP8 block mode: act quantised by the second block's quantiser warps, or by "
+                         "coda_quantize_e4m3 between the blocks")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "aux"], default="forward",
                     help="backward: gradients of the LLaMA-8B chain from a saved forward state; aux: GB/s of the "
                          "memory-bound kernels (fold, reduce, amax, quantise, RMSNorm backward)")

@@ -67,6 +67,11 @@ SIGNATURES = {
     "coda_rmsnorm_backward": (_i32, [_vp, _vp, _fp, _fp, _fp, _vp, _vp, _vp, _fp, _fp, _i64, _i64, _vp]),
     "coda_gemm_swiglu_backward": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
     "coda_gemm_swiglu_save": (_i32, [_vp, _vp, _vp, _fp, _fp, _f32, _fp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
+    "coda_block_fp8_workspace_bytes": (_i64, [_i64]),
+    "coda_block_swiglu_fp8": (_i32, [_vp, _fp, _vp, _fp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _f32, _vp, _fp, _fp, _fp,
+                                     _vp, _fp, _vp, _fp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "coda_block_rowscale_fp8": (_i32, [_vp, _fp, _vp, _fp, _vp, _fp, _vp, _vp, _fp, _f32, _vp, _fp, _fp, _fp, _vp, _fp,
+                                       _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "coda_amax": (_i32, [_vp, _i64, _i32, _fp, _vp]),
     "coda_quantize_e4m3": (_i32, [_vp, _i64, _i32, _fp, _vp, _fp, _vp]),
     "coda_selftest_wait_timeout": (_i32, [_i64, _vp]),
@@ -398,6 +403,77 @@ def coda_block_swiglu_noalloc(X, W1t, R, Wgt, Wut, eps: float, H=None, P=None, A
                                          _dev(Wut, "Wut"), float(eps), _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"),
                                          _dev(Act, "Act"), M, N, K, I, code, _stream(X, stream)))
     return H, P, Act
+
+
+def coda_block_fp8_workspace_bytes(M: int) -> int:
+    return int(load_library().coda_block_fp8_workspace_bytes(M))
+
+
+def block_fp8_workspace(M: int, device) -> torch.Tensor:
+    """A zeroed workspace for the FP8 one-launch blocks (calls leave it zeroed)."""
+    n = coda_block_fp8_workspace_bytes(M)
+    return torch.zeros((n + 3) // 4, dtype=torch.int32, device=device)
+
+
+def _fp8_block_buffers(M, N, K, n_out, dev, A, Aq, scale_a, H, P, amax_h, Hq, scale_h, out):
+    f32, bf, u8 = torch.float32, torch.bfloat16, torch.uint8
+    e = lambda *shape, dt: torch.empty(*shape, dtype=dt, device=dev)  # noqa: E731
+    if A is not None:  # the launch quantises A: it writes Aq and scale_a
+        Aq = e(M, K, dt=u8) if Aq is None else Aq
+        scale_a = e(1, dt=f32) if scale_a is None else scale_a
+    elif Aq is None or scale_a is None:
+        raise ValueError("without A, Aq and scale_a (the e4m3 operand and its scale) must be given")
+    return (Aq, scale_a, e(M, N, dt=bf) if H is None else H,
+            e(M, max(coda_partial_cols(N), 0), dt=f32) if P is None else P, e(1, dt=f32) if amax_h is None else amax_h,
+            e(M, N, dt=u8) if Hq is None else Hq, e(1, dt=f32) if scale_h is None else scale_h,
+            e(M, n_out, dt=bf) if out is None else out)
+
+
+def coda_block_swiglu_fp8(A, amax_a, W1t, scale_w1, R, Wgt, scale_wg, Wut, scale_wu, eps: float, workspace,
+                          Aq=None, scale_a=None, H=None, P=None, r_out=None, amax_h=None, Hq=None, scale_h=None,
+                          Act=None, amax_act=None, M=None, stream=None):
+    """FP8 one-launch block: [Aq = e4m3(A)], h = R + Aq W1, Hq = e4m3(h), Act =
+    silu(r Hq Wg) * (r Hq Wu).  A (bf16) may be None when Aq and scale_a are
+    given.  Returns a dict of the outputs (Aq, scale_a, h, P, amax_h, Hq,
+    scale_h, act, amax_act)."""
+    lib = load_library()
+    src = A if A is not None else Aq
+    M, K = src.shape
+    N, I = W1t.shape[0], Wgt.shape[0]
+    dev = src.device
+    Aq, scale_a, H, P, amax_h, Hq, scale_h, Act = _fp8_block_buffers(M, N, K, I, dev, A, Aq, scale_a, H, P, amax_h,
+                                                                      Hq, scale_h, Act)
+    _check(lib.coda_block_swiglu_fp8(_dev(A, "A"), _dev(amax_a, "amax_a"), _dev(Aq, "Aq"), _dev(scale_a, "scale_a"),
+                                     _dev(W1t, "W1t"), _dev(scale_w1, "scale_w1"), _dev(R, "R"), _dev(Wgt, "Wgt"),
+                                     _dev(scale_wg, "scale_wg"), _dev(Wut, "Wut"), _dev(scale_wu, "scale_wu"),
+                                     float(eps), _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"),
+                                     _dev(amax_h, "amax_h"), _dev(Hq, "Hq"), _dev(scale_h, "scale_h"), _dev(Act, "Act"),
+                                     _dev(amax_act, "amax_act"), M, N, K, I, _dev(workspace, "workspace"),
+                                     _stream(src, stream)))
+    return {"Aq": Aq, "scale_a": scale_a, "h": H, "P": P, "amax_h": amax_h, "Hq": Hq, "scale_h": scale_h,
+            "act": Act, "amax_act": amax_act}
+
+
+def coda_block_rowscale_fp8(A, amax_a, W1t, scale_w1, R, W2t, scale_w2, eps: float, workspace, Aq=None,
+                            scale_a=None, H=None, P=None, r_out=None, amax_h=None, Hq=None, scale_h=None, Z=None,
+                            stream=None):
+    """FP8 one-launch block: [Aq = e4m3(A)], h = R + Aq W1, Hq = e4m3(h), Z =
+    diag(r) Hq W2.  Returns a dict of the outputs (Aq, scale_a, h, P, amax_h,
+    Hq, scale_h, Z)."""
+    lib = load_library()
+    src = A if A is not None else Aq
+    M, K = src.shape
+    N, N2 = W1t.shape[0], W2t.shape[0]
+    dev = src.device
+    Aq, scale_a, H, P, amax_h, Hq, scale_h, Z = _fp8_block_buffers(M, N, K, N2, dev, A, Aq, scale_a, H, P, amax_h,
+                                                                    Hq, scale_h, Z)
+    _check(lib.coda_block_rowscale_fp8(_dev(A, "A"), _dev(amax_a, "amax_a"), _dev(Aq, "Aq"), _dev(scale_a, "scale_a"),
+                                       _dev(W1t, "W1t"), _dev(scale_w1, "scale_w1"), _dev(R, "R"), _dev(W2t, "W2t"),
+                                       _dev(scale_w2, "scale_w2"), float(eps), _dev(H, "H"), _dev(P, "P"),
+                                       _dev(r_out, "r_out"), _dev(amax_h, "amax_h"), _dev(Hq, "Hq"),
+                                       _dev(scale_h, "scale_h"), _dev(Z, "Z"), M, N, K, N2,
+                                       _dev(workspace, "workspace"), _stream(src, stream)))
+    return {"Aq": Aq, "scale_a": scale_a, "h": H, "P": P, "amax_h": amax_h, "Hq": Hq, "scale_h": scale_h, "Z": Z}
 
 
 def coda_amax(x, amax=None, stream=None):

@@ -12,6 +12,9 @@ epilogue"; SwiGLU gate/up from the same section and "five blocks"):
                   h1 = R + X Wo ; r1 ; act = SwiGLU(r1, h1) ;
                   h2 = h1 + act Wd ; r2 ; Z = diag(r2) h2 Wq'          (6 launches)
   full_chain_fp8  the same with every GEMM operand in per-tensor-scaled e4m3
+  full_chain_fp8_blocks  the FP8 chain as amax(X) and two FP8 one-launch
+                  blocks, which quantise X, h1, act and h2 themselves
+                  (3 launches)
   full_chain_train_forward / full_chain_backward, rowscale_block_backward
                   the training forward that saves G || U and r, and the
                   backward from that state (12 launches for the full chain)
@@ -29,9 +32,9 @@ from typing import Dict, Optional
 
 import torch
 
-from . import (coda_amax, coda_fold_gamma, coda_gemm_residual_partial_rms, coda_gemm_rowscale,
-               coda_gemm_rowscale_fused_rms, coda_gemm_swiglu, coda_gemm_swiglu_fused_rms, coda_quantize_e4m3,
-               coda_rms_reduce)
+from . import (coda_amax, coda_block_rowscale_fp8, coda_block_swiglu_fp8, coda_fold_gamma,
+               coda_gemm_residual_partial_rms, coda_gemm_rowscale, coda_gemm_rowscale_fused_rms, coda_gemm_swiglu,
+               coda_gemm_swiglu_fused_rms, coda_quantize_e4m3, coda_rms_reduce)
 
 
 def _b(bufs, key):
@@ -135,6 +138,44 @@ def full_chain_fp8(X, R, Wq8: Dict[str, tuple], eps: float, bufs: Optional[dict]
     Z, r2 = _rowscale(h2q, Wq, P2, eps, b, "r2", "Z", fused_reduce, scale_h=s3, scale_w=sq)
     b.update({"Xq": Xq, "sx": sx, "h1": h1, "P1": P1, "r1": r1, "h1q": h1q, "s1": s1, "act": act, "actq": actq,
               "s2": s2, "h2": h2, "P2": P2, "r2": r2, "h2q": h2q, "s3": s3, "Z": Z})
+    return b
+
+
+def full_chain_fp8_blocks(X, R, Wq8: Dict[str, tuple], eps: float, workspace, bufs: Optional[dict] = None,
+                          quantize_x_in_block: bool = True) -> dict:
+    """The FP8 chain of ``full_chain_fp8`` in two FP8 one-launch blocks:
+    amax(X); block 1 quantises X (or takes it from coda_quantize_e4m3 when
+    quantize_x_in_block is False), runs Wo + residual, quantises h1 and runs
+    gate/up SwiGLU; block 2 quantises act (its amax from block 1), runs the
+    down projection with R = h1, quantises h2 and runs QKV.  Results equal
+    ``full_chain_fp8``'s bit for bit.  ``workspace``: block_fp8_workspace(M)."""
+    b = bufs if bufs is not None else {}
+    dev = X.device
+    for k in ("ax", "a1", "a2", "a3", "sx", "s1", "s2", "s3"):
+        if k not in b:
+            b[k] = torch.empty(1, dtype=torch.float32, device=dev)
+    for k in ("r1", "r2"):
+        if k not in b:
+            b[k] = torch.empty(X.shape[0], dtype=torch.float32, device=dev)
+    Wo, so = Wq8["Wot"]
+    Wg, sg = Wq8["Wgt"]
+    Wu, su = Wq8["Wut"]
+    Wd, sd = Wq8["Wdt"]
+    Wq, sq = Wq8["Wqt"]
+    coda_amax(X, b["ax"])
+    if quantize_x_in_block:
+        xa = {"A": X, "amax_a": b["ax"], "Aq": b.get("Xq"), "scale_a": b["sx"]}
+    else:
+        Xq, sx = coda_quantize_e4m3(X, b["ax"], b.get("Xq"), b["sx"])
+        xa = {"A": None, "amax_a": None, "Aq": Xq, "scale_a": sx}
+    o1 = coda_block_swiglu_fp8(xa["A"], xa["amax_a"], Wo, so, R, Wg, sg, Wu, su, eps, workspace, Aq=xa["Aq"],
+                               scale_a=xa["scale_a"], H=b.get("h1"), P=b.get("P1"), r_out=b.get("r1"),
+                               amax_h=b["a1"], Hq=b.get("h1q"), scale_h=b["s1"], Act=b.get("act"), amax_act=b["a2"])
+    o2 = coda_block_rowscale_fp8(o1["act"], b["a2"], Wd, sd, o1["h"], Wq, sq, eps, workspace, Aq=b.get("actq"),
+                                 scale_a=b["s2"], H=b.get("h2"), P=b.get("P2"), r_out=b.get("r2"), amax_h=b["a3"],
+                                 Hq=b.get("h2q"), scale_h=b["s3"], Z=b.get("Z"))
+    b.update({"Xq": o1["Aq"], "h1": o1["h"], "P1": o1["P"], "h1q": o1["Hq"], "act": o1["act"], "actq": o2["Aq"],
+              "h2": o2["h"], "P2": o2["P"], "h2q": o2["Hq"], "Z": o2["Z"]})
     return b
 
 

@@ -810,6 +810,145 @@ coda_status coda_block_swiglu(const void* X, const void* W1t, const void* R, con
                     stream);
 }
 
+int64_t coda_block_fp8_workspace_bytes(int64_t M) {
+  if (M < 0) return -1;
+  return coda::block_counters((M + 127) / 128, true) * static_cast<int64_t>(sizeof(unsigned));
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared by the FP8 one-launch blocks.  Phase A: h = R + dequant(Aq . W1t^T)
+// with P and amax_h; the quantiser warps then write Hq = e4m3(h / scale_h);
+// phase B: the consumer on Hq with the reduction folded in.  With A_bf16
+// given, the quantiser warps first write Aq = e4m3(A / (amax_a / 448)).
+coda_status block_fp8_impl(int epi_b, const void* A_bf16, const float* amax_a, uint8_t* Aq, float* scale_a,
+                           const uint8_t* W1t, const float* scale_w1, const void* R, const uint8_t* Wb,
+                           const float* scale_wb, const uint8_t* Wb2, const float* scale_wb2, float eps, void* H,
+                           float* P, float* r_out, float* amax_h, uint8_t* Hq, float* scale_h, void* Out,
+                           float* amax_out, int64_t M, int64_t N, int64_t K, int64_t N_out, void* workspace,
+                           cudaStream_t stream) {
+  g_msg[0] = 0;
+  const bool swiglu = epi_b == coda::kEpiSwiGLU;
+  TRY(check_gemm_dims(M, N, K, CODA_E4M3, "N"));
+  TRY(check_gemm_dims(M, N_out, N, CODA_E4M3, swiglu ? "I" : "N2"));
+  REQUIRE(std::isfinite(eps) && eps >= 0.0f, "eps must be finite and >= 0");
+  TRY(check_scalar_ptr(amax_h, "amax_h"));
+  if (amax_out) TRY(check_scalar_ptr(amax_out, "amax_act"));
+  if (M == 0) {
+    TRY(zero_scalar(amax_h, stream));
+    return zero_scalar(amax_out, stream);
+  }
+  const bool quant_a = A_bf16 != nullptr;
+  if (quant_a) {
+    TRY(check_ptr(A_bf16, "A"));
+    TRY(check_scalar_ptr(amax_a, "amax_a"));
+  }
+  TRY(check_ptr(Aq, "Aq"));
+  TRY(check_scalar_ptr(scale_a, "scale_a"));
+  TRY(check_ptr(W1t, "W1t"));
+  TRY(check_scalar_ptr(scale_w1, "scale_w1"));
+  TRY(check_ptr(R, "R"));
+  TRY(check_ptr(Wb, swiglu ? "Wgt" : "W2t"));
+  TRY(check_scalar_ptr(scale_wb, swiglu ? "scale_wg" : "scale_w2"));
+  if (swiglu) {
+    TRY(check_ptr(Wb2, "Wut"));
+    TRY(check_scalar_ptr(scale_wb2, "scale_wu"));
+  }
+  TRY(check_ptr(H, "H"));
+  TRY(check_ptr(P, "P"));
+  if (r_out) TRY(check_scalar_ptr(r_out, "r_out"));
+  TRY(check_ptr(Hq, "Hq"));
+  TRY(check_scalar_ptr(scale_h, "scale_h"));
+  TRY(check_ptr(Out, swiglu ? "Act" : "Z"));
+  TRY(check_ptr(workspace, "workspace"));
+  const int64_t T = coda_partial_cols(N);
+  const char* out_name = swiglu ? "Act" : "Z";
+  // the launch writes Aq and scale_a when it quantises A; else it reads them
+  const Range outs[] = {rng("H", H, M * N * 2), rng("P", P, M * T * 4), rng("r_out", r_out, r_out ? M * 4 : 0),
+                        rng("amax_h", amax_h, 4), rng("Hq", Hq, M * N), rng("scale_h", scale_h, 4),
+                        rng(out_name, Out, M * N_out * 2), rng("amax_act", amax_out, amax_out ? 4 : 0),
+                        rng("workspace", workspace, coda_block_fp8_workspace_bytes(M)),
+                        rng("Aq", quant_a ? Aq : nullptr, quant_a ? M * K : 0),
+                        rng("scale_a", quant_a ? scale_a : nullptr, quant_a ? 4 : 0)};
+  const Range ins[] = {rng("A", A_bf16, quant_a ? M * K * 2 : 0), rng("amax_a", amax_a, quant_a ? 4 : 0),
+                       rng("Aq", quant_a ? nullptr : Aq, quant_a ? 0 : M * K),
+                       rng("scale_a", quant_a ? nullptr : scale_a, quant_a ? 0 : 4), rng("W1t", W1t, N * K),
+                       rng("scale_w1", scale_w1, 4), rng("R", R, M * N * 2), rng("W", Wb, N_out * N),
+                       rng("scale_w", scale_wb, 4), rng("Wut", Wb2, Wb2 ? N_out * N : 0),
+                       rng("scale_wu", scale_wb2, Wb2 ? 4 : 0)};
+  TRY(check_overlaps(outs, 11, ins, 11));
+  TRY(zero_scalar(amax_h, stream));
+  TRY(zero_scalar(amax_out, stream));
+  coda::GemmProblem p = {};
+  p.epi = coda::kEpiResidualPartialRms;
+  p.A = Aq;
+  p.B = W1t;
+  p.R = R;
+  p.D = H;
+  p.M = static_cast<int>(M);
+  p.N_out = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.ep.P = P;
+  p.ep.T = static_cast<int>(T);
+  p.ep.scale_a = scale_a;
+  p.ep.scale_b = scale_w1;
+  p.ep.amax_out = amax_h;
+  p.b.epi = epi_b;
+  p.b.A = Hq;
+  p.b.B = Wb;
+  p.b.B2 = Wb2;
+  p.b.D = Out;
+  p.b.N_out = static_cast<int>(N_out);
+  p.b.K = static_cast<int>(N);
+  p.b.ep.P_in = P;
+  p.b.ep.T_in = static_cast<int>(T);
+  p.b.ep.n_norm = static_cast<float>(N);
+  p.b.ep.eps = eps;
+  p.b.ep.r_out = r_out;
+  p.b.ep.scale_a = scale_h;
+  p.b.ep.scale_b = scale_wb;
+  p.b.ep.scale_b2 = scale_wb2;
+  p.b.ep.amax_out = amax_out;
+  p.band_ready = static_cast<unsigned*>(workspace);
+  p.fp8_block = true;
+  p.q.h = H;
+  p.q.hq = Hq;
+  p.q.amax_h = amax_h;
+  p.q.scale_h = scale_h;
+  p.q.a = A_bf16;
+  p.q.aq = Aq;
+  p.q.amax_a = amax_a;
+  p.q.scale_a = scale_a;
+  p.stream = stream;
+  p.pdl = use_pdl();
+  return run_gemm(CODA_E4M3, p);
+}
+
+}  // namespace
+
+extern "C" {
+
+coda_status coda_block_swiglu_fp8(const void* X, const float* amax_x, uint8_t* Xq, float* scale_x, const uint8_t* W1t,
+                                  const float* scale_w1, const void* R, const uint8_t* Wgt, const float* scale_wg,
+                                  const uint8_t* Wut, const float* scale_wu, float eps, void* H, float* P,
+                                  float* r_out, float* amax_h, uint8_t* Hq, float* scale_h, void* Act,
+                                  float* amax_act, int64_t M, int64_t N, int64_t K, int64_t I, void* workspace,
+                                  cudaStream_t stream) {
+  return block_fp8_impl(coda::kEpiSwiGLU, X, amax_x, Xq, scale_x, W1t, scale_w1, R, Wgt, scale_wg, Wut, scale_wu, eps,
+                        H, P, r_out, amax_h, Hq, scale_h, Act, amax_act, M, N, K, I, workspace, stream);
+}
+
+coda_status coda_block_rowscale_fp8(const void* X, const float* amax_x, uint8_t* Xq, float* scale_x,
+                                    const uint8_t* W1t, const float* scale_w1, const void* R, const uint8_t* W2t,
+                                    const float* scale_w2, float eps, void* H, float* P, float* r_out,
+                                    float* amax_h, uint8_t* Hq, float* scale_h, void* Z, int64_t M, int64_t N,
+                                    int64_t K, int64_t N2, void* workspace, cudaStream_t stream) {
+  return block_fp8_impl(coda::kEpiRowScale, X, amax_x, Xq, scale_x, W1t, scale_w1, R, W2t, scale_w2, nullptr, nullptr,
+                        eps, H, P, r_out, amax_h, Hq, scale_h, Z, nullptr, M, N, K, N2, workspace, stream);
+}
+
 coda_status coda_amax(const void* x, int64_t n, coda_dtype dtype, float* amax, cudaStream_t stream) {
   g_msg[0] = 0;
   REQUIRE(dtype == CODA_F32 || dtype == CODA_BF16, "coda_amax: dtype must be CODA_F32 or CODA_BF16");

@@ -13,6 +13,7 @@
 #include <cstdint>
 
 #include "coda_internal.h"
+#include "fp8_e4m3.cuh"
 #include "sm103_ptx.cuh"
 
 namespace coda {
@@ -117,27 +118,6 @@ __global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, i
   if (threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(amax), __float_as_int(m));
 }
 
-__device__ __forceinline__ float e4m3_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
-
-// x / s rounded to nearest, without a divide per element.  With inv the
-// correctly rounded reciprocal of s: q0 = x * inv is within an ulp of x / s,
-// the residual x - s * q0 is exact in one FMA, and q0 + residual * inv rounds
-// to the correctly rounded quotient (Markstein's theorem on FMA division,
-// IBM J. Res. Dev. 34(1), 1990).  It holds while nothing underflows, which the
-// caller ensures by taking this path only for s in [2^-100, 2^100].
-__device__ __forceinline__ float div_rn_by(float x, float s, float inv) {
-  const float q0 = __fmul_rn(x, inv);
-  return fmaf(fmaf(-s, q0, x), inv, q0);
-}
-
-// q = e4m3(x / s), round-to-nearest-even, saturating (cvt ... .satfinite).
-template <bool FAST>
-__device__ __forceinline__ uint16_t to_e4m3x2(float lo, float hi, float s, float inv) {
-  const float a = FAST ? div_rn_by(lo, s, inv) : __fdiv_rn(lo, s);
-  const float b = FAST ? div_rn_by(hi, s, inv) : __fdiv_rn(hi, s);
-  return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-}
-
 // 16 elements per thread: 16 bytes of q.
 template <bool F32, bool FAST>
 __device__ __forceinline__ void quantize_range(const void* __restrict__ x, int64_t n, float s, float inv,
@@ -170,12 +150,7 @@ __device__ __forceinline__ void quantize_range(const void* __restrict__ x, int64
         }
       }
     }
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      o[j] = static_cast<uint32_t>(to_e4m3x2<FAST>(f[4 * j], f[4 * j + 1], s, inv)) |
-             (static_cast<uint32_t>(to_e4m3x2<FAST>(f[4 * j + 2], f[4 * j + 3], s, inv)) << 16);
-    reinterpret_cast<uint4*>(q)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(q)[v] = e4m3x16<FAST>(f, s, inv);
   }
   if (blockIdx.x == 0) {
     for (int64_t i = n16 * 16 + threadIdx.x; i < n; i += blockDim.x) {
@@ -193,7 +168,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* __restrict__ 
   pdl_wait();
   const float s = e4m3_scale(*amax);
   if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
-  if (s >= 0x1p-100f && s <= 0x1p100f) {  // uniform over the launch
+  if (e4m3_fast_scale(s)) {  // uniform over the launch
     quantize_range<F32, true>(x, n, s, __frcp_rn(s), q);
   } else {
     quantize_range<F32, false>(x, n, s, 0.0f, q);

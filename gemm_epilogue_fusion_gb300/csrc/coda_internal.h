@@ -82,6 +82,31 @@ struct PhaseB {
   EpiParams ep = {};
 };
 
+// FP8 one-launch block: the e4m3 copies that the launch itself makes.  h
+// (phase A's bf16 output) is quantised once every phase-A tile has stored it
+// and folded its |h| into amax_h; with `a` set, phase A's A operand is
+// quantised from its bf16 source first (amax_a final before the launch).
+// Both run in the quantiser warps, band by band, so the consuming GEMM
+// starts on a band as soon as its e4m3 copy is complete.
+struct QuantArgs {
+  const void* h = nullptr;        // h [M, N] bf16: phase A's output
+  uint8_t* hq = nullptr;          // its e4m3 copy: phase B's A operand
+  float* amax_h = nullptr;        // max |h| (zeroed before the launch)
+  float* scale_h = nullptr;       // written: amax_h / 448 (1 if zero)
+  const void* a = nullptr;        // nullable: bf16 source of phase A's A operand [M, K]
+  uint8_t* aq = nullptr;          // its e4m3 copy: phase A's A operand
+  const float* amax_a = nullptr;  // max |a|
+  float* scale_a = nullptr;       // written: amax_a / 448
+};
+
+// Counters of a two-phase launch's workspace, in units of unsigned, for m
+// row bands: [0, m) band ready (h and P stored), [m] CTAs done (the last one
+// resets every counter); FP8 blocks add [m + 1] CTAs past phase A, [m + 2,
+// 2m + 2) bands of h quantised, [2m + 2, 3m + 2) bands of A quantised.
+__host__ __device__ constexpr int64_t block_counters(int64_t m_bands, bool fp8) {
+  return fp8 ? 3 * m_bands + 2 : m_bands + 1;
+}
+
 struct GemmProblem {
   int epi;                 // Epilogue
   const void* A;           // [M, K] K-major activations
@@ -97,7 +122,9 @@ struct GemmProblem {
   bool a_mn = false;       // A stored [K, M] (MN-major) instead of [M, K]
   bool b_mn = false;       // B stored [K, N_out] instead of [N_out, K]
   PhaseB b;                // consuming GEMM of a two-phase launch
-  unsigned* band_ready;    // two-phase: [ceil(M / tile rows) + 1] zeroed counters
+  unsigned* band_ready;    // two-phase: block_counters(ceil(M / tile rows), fp8) zeroed counters
+  bool fp8_block = false;  // two-phase e4m3: h quantised in the launch (QuantArgs)
+  QuantArgs q;
 };
 
 // One launcher per operand kind; each lives in its own translation unit so

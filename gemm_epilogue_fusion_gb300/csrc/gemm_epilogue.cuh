@@ -60,6 +60,7 @@
 #include <type_traits>
 
 #include "coda_internal.h"
+#include "fp8_e4m3.cuh"
 #include "sm103_ptx.cuh"
 
 namespace coda {
@@ -102,9 +103,14 @@ __host__ __device__ constexpr int raster_rows(int epi) {
 }
 
 template <int KIND, int EPI_A, int EPI_B, int STAGES_, int NSLOTS_, int CG_ = 1, bool A_MN_ = false,
-          bool B_MN_ = false>
+          bool B_MN_ = false, int QUANT_ = 0>
 struct GemmCfg {
   static constexpr int kKind = KIND;
+  // FP8 one-launch block: 1 = h quantised between the phases; 2 = phase A's
+  // A operand quantised first as well.  Quantiser warps 7.. do both.
+  static constexpr int QUANT = QUANT_;
+  static constexpr bool FP8_BLOCK = QUANT_ > 0;
+  static constexpr int NUM_QUANT_WARPS = FP8_BLOCK ? 4 : 0;
   // MN-major operands: A stored [K, M] (m contiguous) / B stored [K, N], loaded
   // as 64-element-wide TMA boxes of BK k-rows each
   static constexpr bool A_MN = A_MN_;
@@ -145,7 +151,8 @@ struct GemmCfg {
   static constexpr int SLOT_BYTES = BM * 128;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int NUM_EPI_THREADS = 128;
-  static constexpr int NUM_THREADS = HAS_LOADER ? 224 : 192;
+  static constexpr int NUM_THREADS = (HAS_LOADER ? 224 : 192) + 32 * NUM_QUANT_WARPS;
+  static constexpr int QUANT_WARP0 = 7;
   // shared memory: [A stages][B stages][slots][barriers][tmem slot, abort flag]
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_SLOTS = OFF_B + STAGES * B_BYTES;
@@ -167,8 +174,105 @@ struct GemmCfg {
   static_assert(!(A_MN || B_MN) || (KIND == kKindBF16 && !TWO_PHASE), "MN-major operands: bf16, one phase");
   static_assert((EPI_A != kEpiGradNorm && EPI_A != kEpiSwiGLUBwd) || (KIND == kKindBF16 && NSLOTS % 2 == 0),
                 "backward programs: bf16, an even slot ring");
+  static_assert(!FP8_BLOCK || (KIND == kKindE4M3 && TWO_PHASE && HAS_LOADER), "FP8 blocks: e4m3, two phases");
   static constexpr uint32_t IDESC = make_idesc(FMT, FMT, TILE_M, BN, A_MN, B_MN);
 };
+
+// Elements of one quantiser chunk: 32 lanes x 6 groups of 16 elements.
+constexpr int kQuantGroups = 6;
+constexpr int64_t kQuantChunk = 32 * 16 * kQuantGroups;
+// Chunks per row band of band_rows rows and `cols` columns (the last band
+// counts as many, its chunks past row M being empty).
+__host__ __device__ inline int quant_chunks_per_band(int band_rows, int cols) {
+  return static_cast<int>((static_cast<int64_t>(band_rows) * cols + kQuantChunk - 1) / kQuantChunk);
+}
+
+// One quantiser warp's share of a bf16 [M, cols] tensor -> e4m3 bytes: chunk
+// j (band j / cpb) for j = w, w + nw, ...; each chunk's bytes are made
+// visible (to the TMA loads of other CTAs too) before its band's counter is
+// released.  Software-pipelined: the loads of the next chunk are in flight
+// while the current one is converted, stored and fenced.  cols is a multiple
+// of 16, so a group of 16 elements never crosses a row band's end.  Returns
+// false if the launch was aborted.
+struct QuantChunk {
+  int64_t e0, e_end, band;  // first element of this lane, end of its band, band
+};
+__device__ __forceinline__ QuantChunk quant_chunk(int64_t j, int cpb, int64_t band_elems, int64_t total) {
+  const int lane = threadIdx.x & 31;
+  const int64_t b = j / cpb;
+  const int64_t e_band = b * band_elems;
+  return {e_band + (j - b * cpb) * kQuantChunk + 16 * lane, min(e_band + band_elems, total), b};
+}
+// The bf16 source is read once: streaming loads (evict first), so the
+// stream does not push the GEMM's operand panels out of L2.
+#ifndef CODA_QUANT_STREAMING
+#define CODA_QUANT_STREAMING 1
+#endif
+__device__ __forceinline__ uint4 quant_ld(const uint4* p) {
+#if CODA_QUANT_STREAMING
+  return __ldcs(p);
+#else
+  return __ldcg(p);
+#endif
+}
+__device__ __forceinline__ void quant_load(const __nv_bfloat16* __restrict__ src, const QuantChunk& c,
+                                           uint4 (&v)[kQuantGroups][2]) {
+#pragma unroll
+  for (int g = 0; g < kQuantGroups; ++g) {
+    const int64_t e = c.e0 + 512 * g;
+    if (e < c.e_end) {
+      const uint4* p = reinterpret_cast<const uint4*>(src + e);
+      v[g][0] = quant_ld(p);
+      v[g][1] = quant_ld(p + 1);
+    }
+  }
+}
+template <bool FAST>
+__device__ __forceinline__ bool quantize_bands(const __nv_bfloat16* __restrict__ src, uint8_t* __restrict__ dst,
+                                               int M, int cols, int band_rows, float s, float inv,
+                                               unsigned* ready, int w, int nw, volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int64_t band_elems = static_cast<int64_t>(band_rows) * cols;
+  const int cpb = quant_chunks_per_band(band_rows, cols);
+  const int64_t total = static_cast<int64_t>(M) * cols;
+  const int64_t n_chunks = static_cast<int64_t>((M + band_rows - 1) / band_rows) * cpb;
+  if (w >= n_chunks) return true;
+  uint4 cur[kQuantGroups][2], nxt[kQuantGroups][2];
+  QuantChunk c = quant_chunk(w, cpb, band_elems, total);
+  quant_load(src, c, cur);
+  for (int64_t j = w; j < n_chunks; j += nw) {
+    if (*abort_flag) return false;
+    const bool more = j + nw < n_chunks;
+    QuantChunk cn = c;
+    if (more) {
+      cn = quant_chunk(j + nw, cpb, band_elems, total);
+      quant_load(src, cn, nxt);
+    }
+#pragma unroll
+    for (int g = 0; g < kQuantGroups; ++g) {
+      const int64_t e = c.e0 + 512 * g;
+      if (e < c.e_end) {
+        float f[16];
+        bf16x16_to_float(cur[g][0], cur[g][1], f);
+        *reinterpret_cast<uint4*>(dst + e) = e4m3x16<FAST>(f, s, inv);
+      }
+    }
+    // the codes, then the band's counter: generic stores read by TMA loads
+    fence_proxy_async_global();
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(ready + c.band, 1u);
+    if (more) {
+#pragma unroll
+      for (int g = 0; g < kQuantGroups; ++g) {
+        cur[g][0] = nxt[g][0];
+        cur[g][1] = nxt[g][1];
+      }
+      c = cn;
+    }
+  }
+  return true;
+}
 
 struct TileCoord {
   int m, n;
@@ -317,7 +421,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                          const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmA_b,
                          const __grid_constant__ CUtensorMap tmB_b, const __grid_constant__ CUtensorMap tmB2_b,
                          const __grid_constant__ CUtensorMap tmD_b, int M, PhaseArgs pa, PhaseArgs pb,
-                         unsigned* band_ready) {
+                         unsigned* band_ready, const QuantArgs qa) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -354,6 +458,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   // a band is ready for phase B when every phase-A tile of it (one increment
   // per CTA) has stored h and P
   const unsigned band_target = static_cast<unsigned>(n_tiles_a * C::CG);
+  // FP8 blocks: CTAs past phase A, bands of e4m3 h and of e4m3 A complete
+  [[maybe_unused]] unsigned* const a_done = band_ready + m_tiles + 1;
+  [[maybe_unused]] unsigned* const qh_ready = band_ready + m_tiles + 2;
+  [[maybe_unused]] unsigned* const qa_ready = band_ready + 2 * m_tiles + 2;
+  [[maybe_unused]] const unsigned qh_target = static_cast<unsigned>(quant_chunks_per_band(C::TILE_M, pa.N_out));
+  [[maybe_unused]] const unsigned qa_target = static_cast<unsigned>(quant_chunks_per_band(C::TILE_M, pa.K));
+  [[maybe_unused]] const int num_a_tiles = m_tiles * n_tiles_a;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -451,8 +562,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.group_m, pb.group_m);
         const int num_kb = num_kb_of(tl);
         if (C::TWO_PHASE && tl.phase == 1) {
-          // h and P of this band come from other CTAs of this launch
-          if (!wait_band(&band_ready[tl.m], band_target, abort_flag)) break;
+          // h and P of this band come from other CTAs of this launch (FP8:
+          // the e4m3 copy of h, from the quantiser warps)
+          if (!(C::FP8_BLOCK ? wait_band(&qh_ready[tl.m], qh_target, abort_flag)
+                             : wait_band(&band_ready[tl.m], band_target, abort_flag)))
+            break;
+          fence_proxy_async_global();
+        } else if (C::QUANT == 2 && qa.a != nullptr) {
+          // the e4m3 copy of this band's A operand, quantised in this launch
+          if (!wait_band(&qa_ready[tl.m], qa_target, abort_flag)) break;
           fence_proxy_async_global();
         }
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -579,6 +697,33 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         drain_ring(r_full, C::NSLOTS, used, abort_flag);
       }
     }
+  } else if (warp >= C::QUANT_WARP0) {
+    // ---------------------------------------------- quantiser (FP8 blocks) ----
+    // Phase A's A operand first (if the launch quantises it), then h once
+    // every CTA is past phase A.  The warps of all CTAs share each tensor's
+    // chunks round robin in band order, so bands complete roughly in order.
+    if constexpr (C::FP8_BLOCK) {
+      const int w = static_cast<int>(blockIdx.x) * C::NUM_QUANT_WARPS + (warp - C::QUANT_WARP0);
+      const int nw = static_cast<int>(gridDim.x) * C::NUM_QUANT_WARPS;
+      auto quantize = [&](const void* src, uint8_t* dst, int cols, float s, unsigned* ready) {
+        const auto* x = static_cast<const __nv_bfloat16*>(src);
+        return e4m3_fast_scale(s)
+                   ? quantize_bands<true>(x, dst, M, cols, C::TILE_M, s, __frcp_rn(s), ready, w, nw, abort_flag)
+                   : quantize_bands<false>(x, dst, M, cols, C::TILE_M, s, 0.0f, ready, w, nw, abort_flag);
+      };
+      bool qok = true;
+      if (C::QUANT == 2 && qa.a != nullptr) {
+        const float s = e4m3_scale(*qa.amax_a);
+        if (w == 0 && lane == 0) *qa.scale_a = s;
+        qok = quantize(qa.a, qa.aq, pa.K, s, qa_ready);
+      }
+      // h: every CTA has stored its phase-A tiles and folded |h| into amax_h
+      if (qok && wait_band(a_done, gridDim.x, abort_flag)) {
+        const float s = e4m3_scale(*reinterpret_cast<volatile const float*>(qa.amax_h));
+        if (w == 0 && lane == 0) *qa.scale_h = s;
+        (void)quantize(qa.h, qa.hq, pa.N_out, s, qh_ready);
+      }
+    }
   } else {
     // ----------------------------------------------------------- epilogue ----
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -601,8 +746,20 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       const int N_out = ph.N_out;
       float sab = 1.0f, sab2 = 1.0f;
       if constexpr (C::kKind == kKindE4M3) {
-        sab = *ep.scale_a * *ep.scale_b;
-        if constexpr (is_swiglu(EPI)) sab2 = *ep.scale_a * *ep.scale_b2;
+        float sa;
+        if constexpr (C::FP8_BLOCK) {
+          if (tl.phase == 1) {
+            // h's scale: amax_h is final once every CTA is past phase A
+            (void)wait_band(a_done, gridDim.x, abort_flag);
+            sa = e4m3_scale(*reinterpret_cast<volatile const float*>(qa.amax_h));
+          } else {
+            sa = qa.a != nullptr ? e4m3_scale(*qa.amax_a) : *ep.scale_a;
+          }
+        } else {
+          sa = *ep.scale_a;
+        }
+        sab = sa * *ep.scale_b;
+        if constexpr (is_swiglu(EPI)) sab2 = sa * *ep.scale_b2;
       }
       const int row0 = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
       const int row = row0 + row_in_tile;
@@ -611,7 +768,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       if constexpr (EPI != kEpiResidualPartialRms) {
         if (ep.P_in != nullptr) {
           // the auxiliary reduction, folded in: this row's partials -> r
-          if constexpr (C::TWO_PHASE) (void)wait_band(&band_ready[tl.m], band_target, abort_flag);  // acquire P
+          if constexpr (C::FP8_BLOCK) (void)wait_band(a_done, gridDim.x, abort_flag);  // acquire P (all bands)
+          else if constexpr (C::TWO_PHASE) (void)wait_band(&band_ready[tl.m], band_target, abort_flag);  // acquire P
           rs = row < M ? row_rstd(ep.P_in + static_cast<int64_t>(row) * ep.T_in, ep.T_in, ep.n_norm, ep.eps) : 0.0f;
           if (ep.r_out != nullptr && tl.n == 0 && row < M) ep.r_out[row] = rs;
         } else if (ep.r != nullptr) {
@@ -641,7 +799,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       if (!half_valid) {
         release_acc();
         // nothing to store, but the band still counts this CTA's share of the tile
-        if constexpr (C::TWO_PHASE && EPI == kEpiResidualPartialRms)
+        if constexpr (C::TWO_PHASE && !C::FP8_BLOCK && EPI == kEpiResidualPartialRms)
           if (leader) red_release_gpu_add(&band_ready[tl.m], 1u);
         return;
       }
@@ -851,7 +1009,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           sphase ^= 1u;
         }
       }
-      if constexpr (C::TWO_PHASE && EPI == kEpiResidualPartialRms) {
+      if constexpr (C::TWO_PHASE && !C::FP8_BLOCK && EPI == kEpiResidualPartialRms) {
         // h of this tile is in global memory (and P, fenced above): release the band
         if (leader) {
           tma_store_wait_all();
@@ -861,6 +1019,26 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       }
     };
 
+    // FP8 block: once this CTA's last phase-A tile is stored, fold its |h|
+    // into amax_h and count the CTA past phase A (the quantiser warps of
+    // every CTA wait for all of them)
+    [[maybe_unused]] auto publish_phase_a = [&]() {
+      if constexpr (C::FP8_BLOCK) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) atomicMax(reinterpret_cast<int*>(qa.amax_h), __float_as_int(amax));
+        __threadfence();
+        amax = 0.0f;  // from here on: phase B's output
+        named_bar_sync(1, C::NUM_EPI_THREADS);
+        if (leader) {
+          tma_store_wait_all();
+          fence_proxy_async_global();
+          red_release_gpu_add(a_done, 1u);
+        }
+      }
+    };
+    if constexpr (C::FP8_BLOCK)
+      if (walk(0) >= num_a_tiles) publish_phase_a();  // no phase-A tile in this CTA's walk
     for (int k = 0; ok; ++k, ++it) {
       const int t = walk(k);
       if (t >= num_tiles) break;
@@ -874,15 +1052,18 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         if constexpr (C::TWO_PHASE) run_tile(std::integral_constant<int, C::kEpiB>{}, tl, pb, &tmD_b, buf);
       } else {
         run_tile(std::integral_constant<int, C::kEpiA>{}, tl, pa, &tmD, buf);
+        if constexpr (C::FP8_BLOCK)
+          if (ok && walk(k + 1) >= num_a_tiles) publish_phase_a();
       }
     }
-    if (pa.ep.amax_out || pb.ep.amax_out) {
+    // FP8 blocks publish phase A's amax above; the end publishes phase B's
+    float* amax_dst = C::FP8_BLOCK ? pb.ep.amax_out : (pa.ep.amax_out ? pa.ep.amax_out : pb.ep.amax_out);
+    if (amax_dst) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       // non-negative floats order like their bit patterns; one program per
-      // launch has an amax output (two-phase launches have none)
-      float* dst = pa.ep.amax_out ? pa.ep.amax_out : pb.ep.amax_out;
-      if (lane == 0) atomicMax(reinterpret_cast<int*>(dst), __float_as_int(amax));
+      // launch has an amax output (bf16 two-phase launches have none)
+      if (lane == 0) atomicMax(reinterpret_cast<int*>(amax_dst), __float_as_int(amax));
     }
     if (leader) tma_store_wait_all();
   }
@@ -902,8 +1083,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       unsigned* done = band_ready + m_tiles;
       __threadfence();
       if (atomicAdd(done, 1u) == gridDim.x - 1) {
-        for (int i = 0; i < m_tiles; ++i) band_ready[i] = 0u;
-        *done = 0u;
+        const int n = static_cast<int>(block_counters(m_tiles, C::FP8_BLOCK));
+        for (int i = 0; i < n; ++i) band_ready[i] = 0u;
         __threadfence();
       }
     }
@@ -1033,7 +1214,8 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
   PhaseArgs pa = {p.N_out, p.K, p.ep, group_a};
   PhaseArgs pb = {p.b.N_out, p.b.K, p.b.ep, group_b};
   unsigned* band_ready = p.band_ready;
-  void* args[] = {&tmA, &tmB, &tmB2, &tmR, &tmD, &tmA_b, &tmB_b, &tmB2_b, &tmD_b, &M, &pa, &pb, &band_ready};
+  QuantArgs q = p.q;
+  void* args[] = {&tmA, &tmB, &tmB2, &tmR, &tmD, &tmA_b, &tmB_b, &tmB2_b, &tmD_b, &M, &pa, &pb, &band_ready, &q};
   bool refused = false;
   ce = launch_coresident(
       [&](bool coop) {
@@ -1104,12 +1286,31 @@ cudaError_t launch_gemm(const GemmProblem& p, const char** msg) {
       return cudaErrorInvalidValue;
     }
   }
-  if (p.b.epi == kEpiRowScale)
-    return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 5, 4, 2>>(p, msg)
-                : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 3, 4, 1>>(p, msg);
-  if (p.b.epi == kEpiSwiGLU)
-    return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiSwiGLU, 5, 4, 2>>(p, msg)
-                : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiSwiGLU, 3, 4, 1>>(p, msg);
+  if constexpr (KIND == kKindE4M3) {
+    // FP8 two-phase launches quantise h (and optionally phase A's A operand)
+    // in the launch: the FP8 block configurations, with quantiser warps
+    if (p.b.epi != -1 && !p.fp8_block) {
+      *msg = "an e4m3 two-phase launch is an FP8 block";
+      return cudaErrorInvalidValue;
+    }
+    if (p.b.epi == kEpiRowScale)
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 5, 4, 2, false, false, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 3, 4, 1, false, false, 2>>(p, msg);
+    if (p.b.epi == kEpiSwiGLU)
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiSwiGLU, 5, 4, 2, false, false, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiSwiGLU, 3, 4, 1, false, false, 2>>(p, msg);
+  } else {
+    if (p.fp8_block) {
+      *msg = "FP8 blocks take e4m3 operands";
+      return cudaErrorInvalidValue;
+    }
+    if (p.b.epi == kEpiRowScale)
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 5, 4, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiRowScale, 3, 4, 1>>(p, msg);
+    if (p.b.epi == kEpiSwiGLU)
+      return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiSwiGLU, 5, 4, 2>>(p, msg)
+                  : launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kEpiSwiGLU, 3, 4, 1>>(p, msg);
+  }
   switch (p.epi) {
     case kEpiResidualPartialRms:
       return pair ? launch_cfg<GemmCfg<KIND, kEpiResidualPartialRms, kNoPhase, 5, 4, 2>>(p, msg)

@@ -252,6 +252,53 @@ CODA_API coda_status coda_block_swiglu(const void* X, const void* W1t, const voi
                                        int64_t M, int64_t N, int64_t K, int64_t I, coda_dtype dtype, void* workspace,
                                        cudaStream_t stream);
 
+/* FP8 (e4m3) forms of the one-launch blocks (the CODA write-up, section "lazy
+ * tax of large-model training": FP8 GEMMs make the memory-bound neighbours a
+ * larger share of the step, which is what fusing them removes).  Per-tensor
+ * scales s = amax / 448 (1 for an all-zero tensor), codes e4m3(x / s)
+ * rounded to nearest even and saturated, exactly as coda_quantize_e4m3.
+ * One launch computes, for the consumer Z / Act:
+ *   [Aq = e4m3(A / scale_a), scale_a = amax_a / 448]   when A is given
+ *   h = R + scale_a scale_w1 (Aq . W1t^T)              bf16, with P and
+ *   amax_h = max |h|, then scale_h = amax_h / 448, Hq = e4m3(h / scale_h)
+ *   r = 1 / sqrt(sum_g P[i, g] / N + eps)               (r_out, nullable)
+ *   coda_block_rowscale_fp8: Z = r scale_h scale_w2 (Hq . W2t^T)       bf16
+ *   coda_block_swiglu_fp8:   Act = silu(r s_h s_wg (Hq . Wgt^T)) *
+ *                                  (r s_h s_wu (Hq . Wut^T))          bf16,
+ *                            amax_act = max |Act| (nullable)
+ * Results equal the separate calls (coda_quantize_e4m3, the e4m3 residual
+ * GEMM, coda_quantize_e4m3 of h, the e4m3 consumer with the reduction
+ * folded in) bit for bit.  Warps of every CTA quantise h band by band once
+ * every CTA is past the residual GEMM; the consumer starts on a band as soon
+ * as its e4m3 copy is complete.
+ *   A [M, K] bf16, nullable: with A, amax_a (its max |x|, final before the
+ *     call) is read and Aq [M, K] and scale_a are written by the launch;
+ *     without A, Aq and scale_a are the given e4m3 operand and its scale.
+ *   W1t [N, K], W2t [N2, N], Wgt, Wut [I, N]: e4m3 bytes (gamma folded in
+ *     before quantising) with device scalar scales.  R [M, N] bf16.
+ *   Outputs: H [M, N] bf16, P [M, coda_partial_cols(N)] fp32, amax_h, Hq
+ *     [M, N] e4m3, scale_h, Z [M, N2] / Act [M, I] bf16, amax_act; the
+ *     library zeroes amax_h and amax_act itself (asynchronously on stream).
+ *   K, N multiples of 16; N2 / I multiples of 8.
+ *   workspace: coda_block_fp8_workspace_bytes(M) bytes, zeroed before its
+ *     first use and left zeroed by every call; calls sharing it must not
+ *     overlap on the GPU.  Co-residency and bounded waits as for
+ *     coda_block_swiglu (CODA_ERR_TIMEOUT through coda_get_device_status()). */
+CODA_API int64_t coda_block_fp8_workspace_bytes(int64_t M);
+CODA_API coda_status coda_block_swiglu_fp8(const void* A, const float* amax_a, uint8_t* Aq, float* scale_a,
+                                           const uint8_t* W1t, const float* scale_w1, const void* R,
+                                           const uint8_t* Wgt, const float* scale_wg, const uint8_t* Wut,
+                                           const float* scale_wu, float eps, void* H, float* P, float* r_out,
+                                           float* amax_h, uint8_t* Hq, float* scale_h, void* Act, float* amax_act,
+                                           int64_t M, int64_t N, int64_t K, int64_t I, void* workspace,
+                                           cudaStream_t stream);
+CODA_API coda_status coda_block_rowscale_fp8(const void* A, const float* amax_a, uint8_t* Aq, float* scale_a,
+                                             const uint8_t* W1t, const float* scale_w1, const void* R,
+                                             const uint8_t* W2t, const float* scale_w2, float eps, void* H, float* P,
+                                             float* r_out, float* amax_h, uint8_t* Hq, float* scale_h, void* Z,
+                                             int64_t M, int64_t N, int64_t K, int64_t N2, void* workspace,
+                                             cudaStream_t stream);
+
 /* coda_block_swiglu for callers that cannot allocate device memory (no
  * counterpart in the CODA write-ups: it exists for the way some programs
  * manage memory).  Runtimes that own all device memory and give a kernel

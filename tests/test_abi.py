@@ -184,3 +184,31 @@ def test_selftest_timeout_range(lib):
     assert lib.coda_selftest_wait_timeout(999, None) == g.CODA_ERR_INVALID_ARG
     assert lib.coda_selftest_wait_timeout(10_000_000_001, None) == g.CODA_ERR_INVALID_ARG
     assert b"timeout_ns" in lib.coda_last_error()
+
+
+def _fp8_block(lib, M=512, N=256, K=512, N2=384, A_bf16=A, Aq=A + 64 * MB, H=A + 128 * MB, Hq=A + 192 * MB,
+               R=A + 256 * MB, Z=A + 320 * MB, P=A + 384 * MB, W1=A + 448 * MB, W2=A + 512 * MB, ws=A + 576 * MB,
+               amax_h=A + 640 * MB):
+    s = A + 700 * MB  # the scalars: amax_a, scale_a, scale_w1, scale_w2, scale_h
+    return lib.coda_block_rowscale_fp8(A_bf16, s, Aq, s + 16, W1, s + 32, R, W2, s + 48, 1e-5, H, P, None, amax_h, Hq,
+                                       s + 64, Z, M, N, K, N2, ws, None)
+
+
+def test_fp8_blocks_check_their_arguments(lib):
+    """The FP8 one-launch blocks: e4m3 rows of 16 bytes for K and N, scale
+    pointers required, outputs disjoint from inputs; all checked before
+    anything is enqueued (amax_h is zeroed only after the checks)."""
+    assert _fp8_block(lib, K=520) == g.CODA_ERR_INVALID_ARG          # e4m3 A rows: K % 16
+    assert _fp8_block(lib, N=264) == g.CODA_ERR_INVALID_ARG          # e4m3 h rows: N % 16
+    assert _fp8_block(lib, N2=100) == g.CODA_ERR_INVALID_ARG         # bf16 Z rows: N2 % 8
+    assert _fp8_block(lib, Hq=None) == g.CODA_ERR_INVALID_ARG
+    assert b"Hq is NULL" in lib.coda_last_error()
+    assert _fp8_block(lib, ws=None) == g.CODA_ERR_INVALID_ARG
+    assert _fp8_block(lib, Hq=A + 128 * MB) == g.CODA_ERR_INVALID_ARG  # Hq over H
+    assert b"overlap" in lib.coda_last_error()
+    assert _fp8_block(lib, Aq=A + 16) == g.CODA_ERR_INVALID_ARG     # the launch writes Aq over its source A
+    # without A the launch reads Aq: Aq may not be an output's range either
+    assert _fp8_block(lib, A_bf16=None, Aq=A + 128 * MB) == g.CODA_ERR_INVALID_ARG
+    # the FP8 workspace holds three counters per 128-row band and two more
+    assert lib.coda_block_fp8_workspace_bytes(1000) == (3 * 8 + 2) * 4
+    assert lib.coda_block_fp8_workspace_bytes(-1) == -1
