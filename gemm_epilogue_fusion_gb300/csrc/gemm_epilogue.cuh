@@ -65,20 +65,15 @@
 
 namespace coda {
 
-// Tuning: rows of one raster band (consecutive tiles walk the band's M-tiles
-// before moving right), for the SwiGLU programs and for the others, and the
-// L2 eviction policy of the A and B operand loads.
+// Tuning of the legacy raster (kept for the backward's MN-major programs and
+// selectable with CODA_RASTER=legacy): rows of one band of consecutive tiles
+// walking the band's M-tiles before moving right, for the SwiGLU programs and
+// for the others; both operands loaded with the evict-last L2 policy.
 #ifndef CODA_RASTER_ROWS
 #define CODA_RASTER_ROWS 2048
 #endif
 #ifndef CODA_RASTER_ROWS_SWIGLU
 #define CODA_RASTER_ROWS_SWIGLU 4096
-#endif
-#ifndef CODA_L2_POLICY_A
-#define CODA_L2_POLICY_A l2_policy_evict_last()
-#endif
-#ifndef CODA_L2_POLICY_B
-#define CODA_L2_POLICY_B l2_policy_evict_last()
 #endif
 
 // Per-translation-unit device status word (timeouts), read back and cleared
@@ -91,16 +86,23 @@ constexpr int kNoPhase = -1;
 
 // Programs whose B tile is gate rows ++ up rows (N = 128 + 128).
 __host__ __device__ constexpr bool is_swiglu(int epi) { return epi == kEpiSwiGLU || epi == kEpiSwiGLUSave; }
-// Rows of one raster band of a program's tiles.  Each band reads every weight
-// panel of the phase once (and its own activation panels from L2), so a wider
-// band re-reads the weights fewer times, as long as the band's panels still
-// fit in L2.  A SwiGLU tile reads two weight panels (gate and up) per output
-// column block, so its weights dominate: 4096-row bands cut the weight
-// re-reads in half.  For the other programs the weights are small against
-// the activations and 2048-row bands measure faster.
+// Rows of one legacy raster band of a program's tiles.
 __host__ __device__ constexpr int raster_rows(int epi) {
   return is_swiglu(epi) ? CODA_RASTER_ROWS_SWIGLU : CODA_RASTER_ROWS;
 }
+
+// Order of one phase's output tiles and the L2 policy of its operand loads.
+// Consecutive tile indices walk `group` tiles along one dimension before
+// stepping along the other: M-major bands (group M-tiles down a column, then
+// the next column) keep the band's A panels in L2 while the B panels stream
+// past; N-major bands (group N-tiles along a row, then the next row) keep the
+// band's B panels (the weights) and stream A.  The kept operand is loaded
+// evict-last, the streamed one with the streaming policy.
+struct Raster {
+  int group;    // tiles per band along the banded dimension (>= 1)
+  int n_major;  // 1: bands of N-tiles, rows walked in order
+  int keep;     // 0: keep A, stream B; 1: keep B, stream A; 2: both evict-last (legacy)
+};
 
 template <int KIND, int EPI_A, int EPI_B, int STAGES_, int NSLOTS_, int CG_ = 1, bool A_MN_ = false,
           bool B_MN_ = false, int QUANT_ = 0>
@@ -278,14 +280,24 @@ struct TileCoord {
   int m, n;
 };
 
-// Grouped raster: consecutive tile indices walk group_m M-tiles down one
-// column of output tiles before moving right, so the CTAs in flight share a
-// few A and B panels in L2.
-__host__ __device__ __forceinline__ TileCoord tile_coord(int t, int m_tiles, int n_tiles, int group_m) {
-  const int per_group = group_m * n_tiles;
+// Grouped raster: consecutive tile indices walk `group` M-tiles down one
+// column of output tiles before moving right (or, N-major, `group` N-tiles
+// along one row before moving down), so the CTAs in flight share a few A and
+// B panels in L2.
+__host__ __device__ __forceinline__ TileCoord tile_coord(int t, int m_tiles, int n_tiles, int group,
+                                                         int n_major = 0) {
+  if (n_major) {
+    const int per_group = group * m_tiles;
+    const int g = t / per_group;
+    const int first_n = g * group;
+    const int gn = min(group, n_tiles - first_n);
+    const int local = t - g * per_group;
+    return {local / gn, first_n + local % gn};
+  }
+  const int per_group = group * n_tiles;
   const int g = t / per_group;
-  const int first_m = g * group_m;
-  const int gm = min(group_m, m_tiles - first_m);
+  const int first_m = g * group;
+  const int gm = min(group, m_tiles - first_m);
   const int local = t - g * per_group;
   return {first_m + local % gm, local / gm};
 }
@@ -295,14 +307,14 @@ struct Tile {
   int phase;  // 0 = A, 1 = B
   int m, n;
 };
-__host__ __device__ __forceinline__ Tile tile_at(int t, int m_tiles, int n_tiles_a, int n_tiles_b, int group_a,
-                                                  int group_b) {
+__host__ __device__ __forceinline__ Tile tile_at(int t, int m_tiles, int n_tiles_a, int n_tiles_b, Raster ra,
+                                                  Raster rb) {
   const int num_a = m_tiles * n_tiles_a;
   if (t < num_a) {
-    const TileCoord c = tile_coord(t, m_tiles, n_tiles_a, group_a);
+    const TileCoord c = tile_coord(t, m_tiles, n_tiles_a, ra.group, ra.n_major);
     return {0, c.m, c.n};
   }
-  const TileCoord c = tile_coord(t - num_a, m_tiles, n_tiles_b, group_b);
+  const TileCoord c = tile_coord(t - num_a, m_tiles, n_tiles_b, rb.group, rb.n_major);
   return {1, c.m, c.n};
 }
 
@@ -411,7 +423,8 @@ __device__ __forceinline__ bool wait_band(const unsigned* ctr, unsigned target, 
 struct PhaseArgs {
   int N_out, K;
   EpiParams ep;
-  int group_m;  // M-tiles per raster band (>= 1)
+  Raster raster;  // tile order and L2 policy of the operand loads
+  int stream_first;  // the streamed operand is loaded evict-first (else evict-normal)
 };
 
 template <class C>
@@ -515,7 +528,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer ----
     if (lane == 0) {
-      const uint64_t pol_a = CODA_L2_POLICY_A, pol_b = CODA_L2_POLICY_B;
+      // L2 policies: keep (evict-last) for the operand whose panels the band
+      // reuses; the other operand is still shared by the band's tiles in
+      // flight, so it is loaded with the normal policy (or evict-first)
+      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_stream = pa.stream_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+      auto pol_a_of = [&](const Raster& r) { return r.keep == 1 ? pol_stream : pol_keep; };
+      auto pol_b_of = [&](const Raster& r) { return r.keep == 0 ? pol_stream : pol_keep; };
       // the stage's completion is counted on the MMA CTA's barrier
       const uint32_t full0 = C::CG == 2 ? mapa_shared(smem_u32(full), 0) : 0u;
       // Every box of k-block kb of tile tl that this CTA loads: f(map, x, y,
@@ -559,7 +578,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       for (int k = 0; ok; ++k) {
         const int t = walk(k);
         if (t >= num_tiles) break;
-        const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.group_m, pb.group_m);
+        const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.raster, pb.raster);
         const int num_kb = num_kb_of(tl);
         if (C::TWO_PHASE && tl.phase == 1) {
           // h and P of this band come from other CTAs of this launch (FP8:
@@ -573,6 +592,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           if (!wait_band(&qa_ready[tl.m], qa_target, abort_flag)) break;
           fence_proxy_async_global();
         }
+        const Raster& rst = (C::TWO_PHASE && tl.phase == 1) ? pb.raster : pa.raster;
+        const uint64_t pol_a = pol_a_of(rst), pol_b = pol_b_of(rst);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_status)) {
             ok = false;
@@ -615,7 +636,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       for (int k = 0; ok; ++k, ++it) {
         const int t = walk(k);
         if (t >= num_tiles) break;
-        const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.group_m, pb.group_m);
+        const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.raster, pb.raster);
         const int num_kb = (((C::TWO_PHASE && tl.phase == 1) ? pb.K : pa.K) + C::BK - 1) / C::BK;
         const int buf = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
@@ -664,7 +685,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         for (int k = 0; ok; ++k) {
           const int t = walk(k);
           if (t >= num_tiles) break;
-          const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.group_m, pb.group_m);
+          const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.raster, pb.raster);
           const bool pB = C::TWO_PHASE && tl.phase == 1;
           const int row0 = tl.m * C::TILE_M + static_cast<int>(cta_rank) * C::BM;
           if (row0 >= M) continue;  // this CTA's half of the tile is empty
@@ -1042,7 +1063,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     for (int k = 0; ok; ++k, ++it) {
       const int t = walk(k);
       if (t >= num_tiles) break;
-      const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.group_m, pb.group_m);
+      const Tile tl = tile_at(t, m_tiles, n_tiles_a, n_tiles_b, pa.raster, pb.raster);
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1) & 1u;
       // one decision for all 128 threads, so no thread is left at a barrier
@@ -1092,6 +1113,82 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host ----
+
+// L2 bytes a band's kept panels may fill in the CODA_RASTER=auto experiment
+// (CODA_L2_BUDGET_MB, default 64 MB).
+inline int64_t l2_band_budget() {
+  static const int64_t b = [] {
+    const char* e = getenv("CODA_L2_BUDGET_MB");
+    const long mb = e ? atol(e) : 64;
+    return static_cast<int64_t>(mb > 0 ? mb : 64) << 20;
+  }();
+  return b;
+}
+inline int stream_evict_first() {
+  static const int f = [] {
+    const char* e = getenv("CODA_L2_STREAM");
+    return e != nullptr && e[0] == 'f' ? 1 : 0;
+  }();
+  return f;
+}
+inline bool legacy_raster_forced() {
+  static const bool f = [] {
+    const char* e = getenv("CODA_RASTER");
+    return e != nullptr && e[0] == 'l';
+  }();
+  return f;
+}
+inline bool auto_raster() {
+  static const bool f = [] {
+    const char* e = getenv("CODA_RASTER");
+    return e != nullptr && e[0] == 'a';
+  }();
+  return f;
+}
+
+// The tile order of one phase.  The legacy raster (M-major bands of 2048 or
+// 4096 rows, both operands evict-last) measures fastest on most shapes, even
+// where other orders read fewer DRAM bytes: the tiles of a band in flight
+// read each B k-slice together.  One case gains from keeping the weights
+// instead: a long-K phase (at least 8192 bytes of K per row) whose whole
+// weight fits in a 40 MB band.  There, N-major rows with every N-tile in one
+// band read the weight once, and the rows complete in order, so a two-phase
+// launch's consumer starts on early rows sooner (the LLaMA-1B MLP-down block
+// +1.7%, the 8B chain +0.7%).  With shorter K rows the same order measured
+// 1.5% slower (the 1B attention-out Wo); a larger weight does not stay in L2
+// (the 8B down projection's 117 MB weight in 58 MB bands, and M-tile bands
+// kept against evict-first weights, both read more and ran slower).
+// CODA_RASTER=legacy keeps the legacy raster everywhere; CODA_RASTER=auto
+// picks the order with the fewest modelled DRAM bytes in
+// CODA_L2_BUDGET_MB-sized bands (an experiment: slower on most shapes).
+template <class C>
+Raster choose_raster(int M, int N_out, int K, int epi) {
+  if (epi == kNoPhase) return {1, 0, 2};
+  const int g_legacy = raster_rows(epi) / C::TILE_M > 0 ? raster_rows(epi) / C::TILE_M : 1;
+  const Raster legacy = {g_legacy, 0, 2};
+  if (C::A_MN || C::B_MN || legacy_raster_forced()) return legacy;
+  const int64_t m_tiles = (M + C::TILE_M - 1) / C::TILE_M;
+  const int64_t n_tiles = (N_out + C::out_cols(epi) - 1) / C::out_cols(epi);
+  const int64_t k_bytes = static_cast<int64_t>(K) * C::ELEM;
+  const int64_t a_panel = static_cast<int64_t>(C::TILE_M) * k_bytes;  // A rows of one tile
+  const int64_t b_panel = static_cast<int64_t>(C::BN) * k_bytes;      // B rows of one tile (gate + up)
+  if (!auto_raster()) {
+    if (k_bytes >= 8192 && b_panel * n_tiles <= (int64_t(40) << 20)) return {static_cast<int>(n_tiles), 1, 1};
+    return legacy;
+  }
+  const int64_t budget = l2_band_budget();
+  // the most tiles a band may keep, then spread evenly over the bands it takes
+  auto band = [](int64_t g, int64_t n) {
+    g = g < 1 ? int64_t(1) : (g > n ? n : g);
+    const int64_t bands = (n + g - 1) / g;
+    return (n + bands - 1) / bands;
+  };
+  const int64_t gm = band(budget / a_panel, m_tiles), gn = band(budget / b_panel, n_tiles);
+  const int64_t bytes_m = a_panel * m_tiles + b_panel * n_tiles * ((m_tiles + gm - 1) / gm);
+  const int64_t bytes_n = b_panel * n_tiles + a_panel * m_tiles * ((n_tiles + gn - 1) / gn);
+  if (bytes_n < bytes_m || (gn == n_tiles && bytes_n == bytes_m)) return {static_cast<int>(gn), 1, 1};
+  return {static_cast<int>(gm), 0, 0};
+}
 
 template <class C>
 cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
@@ -1209,10 +1306,9 @@ cudaError_t launch_cfg(const GemmProblem& p, const char** msg) {
   // grid never exceeds the co-resident units
   const int grid = C::CG * (num_tiles < units ? num_tiles : units);
   int M = p.M;
-  constexpr int group_a = raster_rows(C::kEpiA) / C::TILE_M > 0 ? raster_rows(C::kEpiA) / C::TILE_M : 1;
-  constexpr int group_b = raster_rows(C::kEpiB) / C::TILE_M > 0 ? raster_rows(C::kEpiB) / C::TILE_M : 1;
-  PhaseArgs pa = {p.N_out, p.K, p.ep, group_a};
-  PhaseArgs pb = {p.b.N_out, p.b.K, p.b.ep, group_b};
+  PhaseArgs pa = {p.N_out, p.K, p.ep, choose_raster<C>(p.M, p.N_out, p.K, C::kEpiA), stream_evict_first()};
+  PhaseArgs pb = {p.b.N_out, p.b.K, p.b.ep, choose_raster<C>(p.M, p.b.N_out, p.b.K, C::kEpiB),
+                  stream_evict_first()};
   unsigned* band_ready = p.band_ready;
   QuantArgs q = p.q;
   void* args[] = {&tmA, &tmB, &tmB2, &tmR, &tmD, &tmA_b, &tmB_b, &tmB2_b, &tmD_b, &M, &pa, &pb, &band_ready, &q};

@@ -23,10 +23,10 @@ PROGRAM = r"""
 using coda::walk_tile;
 using coda::tile_at;
 // 0 if tile_at maps phase A's and phase B's indices one to one onto their grids
-static int check_raster(int m_tiles, int n_a, int n_b, int g_a, int g_b) {
+static int check_raster(int m_tiles, int n_a, int n_b, int g_a, int g_b, int nm_a = 0, int nm_b = 0) {
   std::vector<int> seen_a(m_tiles * n_a, 0), seen_b(m_tiles * n_b, 0);
   for (int t = 0; t < m_tiles * (n_a + n_b); ++t) {
-    const coda::Tile c = tile_at(t, m_tiles, n_a, n_b, g_a, g_b);
+    const coda::Tile c = tile_at(t, m_tiles, n_a, n_b, coda::Raster{g_a, nm_a, 0}, coda::Raster{g_b, nm_b, 0});
     const int nn = c.phase ? n_b : n_a;
     if (c.phase != (t >= m_tiles * n_a) || c.m < 0 || c.m >= m_tiles || c.n < 0 || c.n >= nn) return 1;
     (c.phase ? seen_b : seen_a)[c.m * nn + c.n]++;
@@ -64,7 +64,32 @@ int main() {
       for (int nb = 0; nb <= 70; nb += 23)
         for (int ga = 1; ga <= 34; ga += 3)
           for (int gb = 1; gb <= 34; gb += 4)
-            if (check_raster(m, na, nb, ga, gb)) { printf("FAIL raster m=%d na=%d nb=%d ga=%d gb=%d\n", m, na, nb, ga, gb); return 1; }
+            for (int nm = 0; nm < 4; ++nm)
+              if (check_raster(m, na, nb, ga, gb, nm & 1, nm >> 1)) { printf("FAIL raster m=%d na=%d nb=%d ga=%d gb=%d nm=%d\n", m, na, nb, ga, gb, nm); return 1; }
+  // N-major bands walk rows in order: the first n tiles of a band are row 0
+  {
+    const coda::TileCoord c0 = coda::tile_coord(0, 10, 16, 8, 1), c7 = coda::tile_coord(7, 10, 16, 8, 1),
+                          c8 = coda::tile_coord(8, 10, 16, 8, 1), c80 = coda::tile_coord(80, 10, 16, 8, 1);
+    if (c0.m != 0 || c0.n != 0 || c7.m != 0 || c7.n != 7 || c8.m != 1 || c8.n != 0 || c80.m != 0 || c80.n != 8) {
+      printf("FAIL n-major order\n"); return 1;
+    }
+  }
+  // the raster chosen for each phase of the LLaMA blocks (bf16, CTA pairs):
+  // group, n_major, keep (0: keep A, 1: keep B)
+  {
+    using Res = coda::GemmCfg<coda::kKindBF16, coda::kEpiResidualPartialRms, coda::kNoPhase, 5, 4, 2>;
+    using Sw = coda::GemmCfg<coda::kKindBF16, coda::kEpiSwiGLU, coda::kNoPhase, 6, 2, 2>;
+    using Rs = coda::GemmCfg<coda::kKindBF16, coda::kEpiRowScale, coda::kNoPhase, 6, 2, 2>;
+    const coda::Raster r[] = {
+        coda::choose_raster<Res>(16384, 4096, 4096, coda::kEpiResidualPartialRms),   // 8B Wo
+        coda::choose_raster<Sw>(16384, 14336, 4096, coda::kEpiSwiGLU),               // 8B gate/up
+        coda::choose_raster<Res>(16384, 4096, 14336, coda::kEpiResidualPartialRms),  // 8B down
+        coda::choose_raster<Rs>(16384, 6144, 4096, coda::kEpiRowScale),              // 8B QKV
+        coda::choose_raster<Res>(8192, 2048, 8192, coda::kEpiResidualPartialRms),    // 1B MLP-down
+        coda::choose_raster<Rs>(8192, 3072, 2048, coda::kEpiRowScale),               // 1B QKV
+        coda::choose_raster<Sw>(8192, 8192, 2048, coda::kEpiSwiGLU)};                // 1B gate/up
+    for (const auto& x : r) printf("raster group=%d n_major=%d keep=%d\n", x.group, x.n_major, x.keep);
+  }
   for (int U = 1; U < 160; U += 3)
     for (int nA = 0; nA < 700; nA += 41)
       for (int nB = 0; nB < 900; nB += 67)
@@ -101,3 +126,13 @@ def test_walk_tile_deals_every_tile_once_in_phase_order(tmp_path):
     lines = [l for l in out.stdout.splitlines() if l.startswith("shape")]
     # the 1B MLP-down + QKV block: 4x longer phase-A tiles, balanced from 672 to 608 k-blocks
     assert "nA=256 nB=384 d=4 max=608 round_robin_max=672" in out.stdout, lines
+    # the raster per phase: a phase with K rows of 8192 bytes or more whose
+    # whole weight fits 40 MB keeps it (N-major rows, every N-tile in one
+    # band): the 8B Wo (33.5 MB) and the 1B MLP-down (33.5 MB); every other
+    # phase keeps the legacy M-major bands (8 M-tiles of 256 rows; 16 for
+    # gate/up)
+    rs = [l for l in out.stdout.splitlines() if l.startswith("raster")]
+    assert rs == ["raster group=16 n_major=1 keep=1", "raster group=16 n_major=0 keep=2",
+                  "raster group=8 n_major=0 keep=2", "raster group=8 n_major=0 keep=2",
+                  "raster group=8 n_major=1 keep=1", "raster group=8 n_major=0 keep=2",
+                  "raster group=16 n_major=0 keep=2"], rs
