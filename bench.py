@@ -85,6 +85,28 @@ def algorithmic_bytes(M, K1, N, I, T):
     return fused, unfused
 
 
+def chain_bytes_full(w, T):
+    """Compulsory HBM bytes of one step of the 8B chain (bf16), fused (the two
+    one-launch blocks: every operand, residual, output, partial and row scale
+    once) and unfused (cuBLAS-style GEMMs with the add, RMSNorm and silu*mul as
+    separate passes, each reading its inputs and writing its output once)."""
+    b, M, H, I, Q, K1 = 2, w.M, w.N, w.inter, w.N2, w.K1
+    fused = (b * (M * K1 + H * K1 + 2 * M * H) + 4 * M * T                  # X, Wo, R -> h1, P1
+             + b * (M * H + 2 * I * H + M * I) + 4 * M * T + 4 * M          # h1, Wg, Wu, P1 -> act, r1
+             + b * (M * I + H * I + 2 * M * H) + 4 * M * T                  # act, Wd, h1 -> h2, P2
+             + b * (M * H + Q * H + M * Q) + 4 * M * T + 4 * M)             # h2, Wq, P2 -> Z, r2
+    unfused = b * (M * K1 + H * K1 + M * H                                  # X Wo -> XW
+                   + 3 * M * H                                              # XW + R -> h1
+                   + 2 * M * H                                              # RMSNorm(h1) -> y1
+                   + M * H + 2 * I * H + 2 * M * I                          # y1 [Wg Wu] -> g, u
+                   + 3 * M * I                                              # silu(g) * u -> act
+                   + M * I + H * I + M * H                                  # act Wd -> AW
+                   + 3 * M * H                                              # AW + h1 -> h2
+                   + 2 * M * H                                              # RMSNorm(h2) -> y2
+                   + M * H + Q * H + M * Q)                                 # y2 Wq -> Z
+    return fused, unfused
+
+
 def timed_kernel_bytes(w, mode, T):
     """Compulsory HBM bytes of one launch of the kernel the roofline reports:
     every operand, residual, output, partial and row scale read or written
@@ -756,6 +778,11 @@ def run_coda(args, w):
     if w.chain == "swiglu":
         fused_b, unfused_b = algorithmic_bytes(w.M, w.K1, w.N, w.N2, g.coda_partial_cols(w.N))
         line["dram_bytes_algorithmic"] = {"fused": sum(fused_b.values()), "unfused": unfused_b}
+    if w.chain == "full" and w.dtype == "bf16":
+        fused_b, unfused_b = chain_bytes_full(w, g.coda_partial_cols(w.N))
+        line["dram_bytes_algorithmic"] = {"fused": fused_b, "unfused": unfused_b,
+                                          "measured_fused": "profiles/ncu_block_swiglu_llama8b_chain.md",
+                                          "measured_unfused": "profiles/dram_fused_vs_unfused_llama8b_chain.md"}
     if not args.no_cpu_baseline:
         n, dt, fl_cpu, threads = oracle_sample(w, inp, args.cpu_budget)
         line["cpu_baseline"] = {"value": fl_cpu / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -921,9 +948,10 @@ def run_unfused_backward(args, w):
 
 
 def run_unfused(args, w):
-    """cuBLAS + PyTorch eager, unfused: XW, add, RMSNorm (fp32 math), GEMM, silu*mul."""
-    if w.chain != "swiglu":
-        raise SystemExit("--impl unfused covers the attention-out + SwiGLU block only")
+    """cuBLAS + PyTorch eager, unfused: XW, add, RMSNorm (fp32 math), GEMM, silu*mul
+    (and, for the 8B chain, the down GEMM, add, RMSNorm and QKV GEMM)."""
+    if w.chain not in ("swiglu", "full") or w.dtype != "bf16":
+        raise SystemExit("--impl unfused covers the bf16 attention-out + SwiGLU block and the bf16 8B chain")
     dist, rank, ws = dist_setup("nccl")
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -931,15 +959,23 @@ def run_unfused(args, w):
     inp = make_inputs(w)
     d = {k: v.to(dev) for k, v in inp.items()}
     Wgu = torch.cat([d["Wgt"], d["Wut"]], 0)
-    gamma = d["gamma1"]
 
-    def step():
-        h = torch.matmul(d["X"], d["W1t"].t()) + d["R"]
+    def rms(h, gamma):
         hf = h.float()
-        y = (hf * torch.rsqrt(hf.pow(2).mean(-1, keepdim=True) + w.eps) * gamma).bfloat16()
-        gu = torch.matmul(y, Wgu.t())
+        return (hf * torch.rsqrt(hf.pow(2).mean(-1, keepdim=True) + w.eps) * gamma).bfloat16()
+
+    def block(X, R):
+        h = torch.matmul(X, d["W1t"].t()) + R
+        gu = torch.matmul(rms(h, d["gamma1"]), Wgu.t())
         g_, u = gu.chunk(2, dim=-1)
         return h, torch.nn.functional.silu(g_) * u
+
+    def step():
+        h, act = block(d["X"], d["R"])
+        if w.chain == "swiglu":
+            return h, act
+        h2 = torch.matmul(act, d["Wdt"].t()) + h
+        return h2, torch.matmul(rms(h2, d["gamma2"]), d["Wqt"].t())
 
     if args.compile:
         _compile_toolchain()

@@ -81,3 +81,15 @@ def test_default_workload_is_the_8b_chain(monkeypatch):
     bench.main()
     assert seen["w"].name == "llama8b_chain" and seen["args"].reduce in ("auto", "block")
     assert seen["args"].sustained_s >= 2.0
+
+
+def test_chain_bytes_of_the_8b_chain():
+    """The 8B chain's compulsory bytes: 2525.1 MB through the two one-launch
+    blocks against 5469.4 MB for the unfused sequence (2.17x)."""
+    from coda_inputs import WORKLOADS
+    fused, unfused = bench.chain_bytes_full(WORKLOADS["llama8b_chain"], 32)
+    assert fused / 1e6 == pytest.approx(2525.1, abs=0.1)
+    assert unfused / 1e6 == pytest.approx(5469.4, abs=0.1)
+    # the first block's share equals the timed kernel's bytes
+    w = WORKLOADS["llama8b_chain"]
+    assert bench.timed_kernel_bytes(w, "block", 32) < fused

@@ -46,6 +46,10 @@ CASES = [
     Workload("block_f32_swiglu", "swiglu", 257, 128, 256, 136, 0, "f32", 1e-5, 53),
     WORKLOADS["llama1b_attn_out_swiglu"].with_rows(1000),
     WORKLOADS["llama1b_mlp_down_qkv"].with_rows(777),
+    # K rows of 8192+ bytes and a small weight: the residual phase walks N-major
+    # rows with the weight kept in L2; ragged M, N and N2 / I
+    Workload("block_ragged_nmajor_rowscale", "rowscale", 600, 4160, 392, 200, 0, "bf16", 1e-5, 54),
+    Workload("block_ragged_nmajor_swiglu", "swiglu", 450, 4104, 264, 136, 0, "bf16", 1e-5, 55),
 ]
 
 
