@@ -67,6 +67,17 @@ def test_fp8_blocks_equal_separate_launches(w, xq, cg, monkeypatch):
     compare(w, {k: v.cpu() for k, v in got.items() if isinstance(v, torch.Tensor)}, oracle_ref(w, inp))
 
 
+@pytest.mark.parametrize("m", [1, 17, 129])
+def test_fp8_blocks_tiny_m(m):
+    """Fewer quantiser chunks than quantiser warps, bands of a few rows, pairs
+    whose second half lies past M: still the separate launches' bits."""
+    w = Workload(f"fp8_block_m{m}", "full", m, 272, 144, 200, 336, "e4m3", 1e-5, 40 + m)
+    d = to_device(make_inputs(w))
+    got, ref = _run_both(w, d, True)
+    for k in KEYS:
+        assert torch.equal(got[k], ref[k]), k
+
+
 def test_fp8_blocks_twice_reuse_the_workspace():
     """Two calls in a row on one workspace (the first leaves it zeroed) and an
     all-zero X (scale 1, every code zero) both come out as the separate calls."""
