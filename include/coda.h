@@ -32,7 +32,8 @@
  * in the QKV GEMM's epilogue (coda_gemm_rowscale_rope), give the backward of
  * the block (coda_gemm_grad_norm, coda_rmsnorm_backward, coda_gemm with
  * either operand layout, coda_gemm_swiglu_save / coda_gemm_swiglu_backward),
- * and quantise to FP8 (coda_amax, coda_quantize_e4m3).
+ * quantise to FP8 (coda_amax, coda_quantize_e4m3), and run an FP8 block in
+ * one launch that quantises its own operands (coda_block_*_fp8).
  *
  * Conventions shared by every call
  *   - Matrices are row-major.  Activations are [rows, K]; a weight W [K, N]
@@ -279,7 +280,8 @@ CODA_API coda_status coda_block_swiglu(const void* X, const void* W1t, const voi
  *   Outputs: H [M, N] bf16, P [M, coda_partial_cols(N)] fp32, amax_h, Hq
  *     [M, N] e4m3, scale_h, Z [M, N2] / Act [M, I] bf16, amax_act; the
  *     library zeroes amax_h and amax_act itself (asynchronously on stream).
- *   K, N multiples of 16; N2 / I multiples of 8.
+ *   K, N multiples of 16; N2 / I multiples of 8.  M = 0 zeroes amax_h and
+ *   amax_act and writes nothing else.
  *   workspace: coda_block_fp8_workspace_bytes(M) bytes, zeroed before its
  *     first use and left zeroed by every call; calls sharing it must not
  *     overlap on the GPU.  Co-residency and bounded waits as for
