@@ -57,6 +57,8 @@ SIGNATURES = {
                                    _vp]),
     "coda_block_swiglu": (_i32, [_vp, _vp, _vp, _vp, _vp, _f32, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _i64, _i32, _vp,
                                  _vp]),
+    "coda_block_rowscale_rope": (_i32, [_vp, _vp, _vp, _vp, _f32, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _i64, _i32,
+                                        _i64, _i64, ctypes.c_double, _i64, _vp, _vp, _vp]),
     "coda_block_swiglu_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _f32, _vp, _fp, _fp, _vp, _i64, _i64, _i64, _i64,
                                          _i32, _vp]),
     "coda_gemm_rowscale_rope": (_i32, [_vp, _vp, _fp, _fp, _f32, _fp, _vp, _i64, _i64, _i64, _i32, _fp, _fp, _i64,
@@ -373,6 +375,22 @@ def coda_block_rowscale(X, W1t, R, W2t, eps: float, workspace, H=None, P=None, Z
     _check(lib.coda_block_rowscale(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(W2t, "W2t"), float(eps),
                                    _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"), _dev(Z, "Z"), M, N, K, N2, code,
                                    _dev(workspace, "workspace"), _stream(X, stream)))
+    return H, P, Z
+
+
+def coda_block_rowscale_rope(X, W1t, R, W2t, eps: float, workspace, head_dim: int, rope_cols: int, base: float, *,
+                             seq_len: int = 0, positions=None, H=None, P=None, Z=None, r_out=None, stream=None):
+    """One launch: h = R + X W1, P, r, Z = RoPE(diag(r) h W2) on the first rope_cols columns.
+    Positions: ``positions`` [M] int32, else row mod ``seq_len``.  Returns (h, P, Z)."""
+    lib = load_library()
+    M, K = X.shape
+    N, N2 = W1t.shape[0], W2t.shape[0]
+    code = _dtype_code(X)
+    H, P, Z = _block_outputs(X, R, N, N2, H, P, Z, code)
+    _check(lib.coda_block_rowscale_rope(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(W2t, "W2t"), float(eps),
+                                        _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"), _dev(Z, "Z"), M, N, K, N2,
+                                        code, head_dim, rope_cols, float(base), seq_len, _dev(positions, "positions"),
+                                        _dev(workspace, "workspace"), _stream(X, stream)))
     return H, P, Z
 
 

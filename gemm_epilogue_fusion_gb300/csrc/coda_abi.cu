@@ -337,6 +337,30 @@ struct RopeArgs {
   const int32_t* positions;
 };
 
+// Checks of the RoPE arguments of a row-scale program with N2 output columns.
+coda_status check_rope(const RopeArgs* rope, int64_t M, int64_t N2, coda_dtype dtype) {
+  const int64_t chunk = 16 / out_bytes(dtype);  // columns per 16-byte store chunk
+  REQUIRE(rope->head_dim > 0 && rope->head_dim % chunk == 0,
+          "head_dim must be a positive multiple of %" PRId64 " for this dtype", chunk);
+  REQUIRE(rope->rope_cols >= 0 && rope->rope_cols <= N2 && rope->rope_cols % rope->head_dim == 0,
+          "rope_cols must be a multiple of head_dim within [0, N2]");
+  REQUIRE(std::isfinite(rope->base) && rope->base > 1.0, "base must be finite and > 1");
+  REQUIRE(rope->positions != nullptr || (rope->seq_len > 0 && rope->seq_len < INT32_MAX),
+          "seq_len must be in [1, 2^31) when positions is NULL");
+  if (M > 0 && rope->positions) TRY(check_scalar_ptr(rope->positions, "positions"));
+  return CODA_OK;
+}
+
+// The RoPE fields of a row-scale program's epilogue.
+void set_rope(coda::EpiParams& ep, const RopeArgs* rope) {
+  if (rope == nullptr || rope->rope_cols <= 0) return;
+  ep.rope_pos = rope->positions;
+  ep.rope_seq = static_cast<int>(rope->positions ? 1 : rope->seq_len);
+  ep.rope_half = static_cast<int>(rope->head_dim / 2);
+  ep.rope_cols = static_cast<int>(rope->rope_cols);
+  ep.rope_log2b = static_cast<float>(std::log2(rope->base) / static_cast<double>(rope->head_dim / 2));
+}
+
 // Shared by the row-scale calls: r given, or reduced in the epilogue from P;
 // optionally RoPE on the leading columns.
 coda_status gemm_rowscale_impl(const void* H, const void* W2t, const float* r, const float* P, float eps,
@@ -344,17 +368,7 @@ coda_status gemm_rowscale_impl(const void* H, const void* W2t, const float* r, c
                                const float* scale_h, const float* scale_w, cudaStream_t stream,
                                const RopeArgs* rope = nullptr) {
   g_msg[0] = 0;
-  if (rope) {
-    const int64_t chunk = 16 / out_bytes(dtype);  // columns per 16-byte store chunk
-    REQUIRE(rope->head_dim > 0 && rope->head_dim % chunk == 0,
-            "head_dim must be a positive multiple of %" PRId64 " for this dtype", chunk);
-    REQUIRE(rope->rope_cols >= 0 && rope->rope_cols <= N2 && rope->rope_cols % rope->head_dim == 0,
-            "rope_cols must be a multiple of head_dim within [0, N2]");
-    REQUIRE(std::isfinite(rope->base) && rope->base > 1.0, "base must be finite and > 1");
-    REQUIRE(rope->positions != nullptr || (rope->seq_len > 0 && rope->seq_len < INT32_MAX),
-            "seq_len must be in [1, 2^31) when positions is NULL");
-    if (M > 0 && rope->positions) TRY(check_scalar_ptr(rope->positions, "positions"));
-  }
+  if (rope) TRY(check_rope(rope, M, N2, dtype));
   TRY(check_gemm_dims(M, N2, K, dtype, "N2"));
   TRY(check_scales(dtype, scale_h, "scale_h", scale_w, "scale_w"));
   if (P) REQUIRE(std::isfinite(eps) && eps >= 0.0f, "eps must be finite and >= 0");
@@ -392,13 +406,7 @@ coda_status gemm_rowscale_impl(const void* H, const void* W2t, const float* r, c
   p.ep.r_out = P ? r_out : nullptr;
   p.ep.scale_a = scale_h;
   p.ep.scale_b = scale_w;
-  if (rope && rope->rope_cols > 0) {
-    p.ep.rope_pos = rope->positions;
-    p.ep.rope_seq = static_cast<int>(rope->positions ? 1 : rope->seq_len);
-    p.ep.rope_half = static_cast<int>(rope->head_dim / 2);
-    p.ep.rope_cols = static_cast<int>(rope->rope_cols);
-    p.ep.rope_log2b = static_cast<float>(std::log2(rope->base) / static_cast<double>(rope->head_dim / 2));
-  }
+  set_rope(p.ep, rope);
   p.stream = stream;
   p.pdl = use_pdl();
   return run_gemm(dtype, p);
@@ -801,6 +809,27 @@ coda_status coda_block_rowscale(const void* X, const void* W1t, const void* R, c
                                 coda_dtype dtype, void* workspace, cudaStream_t stream) {
   return block_impl(coda::kEpiRowScale, X, W1t, R, W2t, nullptr, eps, H, P, r_out, Z, M, N, K, N2, dtype, workspace,
                     stream);
+}
+
+coda_status coda_block_rowscale_rope(const void* X, const void* W1t, const void* R, const void* W2t, float eps,
+                                     void* H, float* P, float* r_out, void* Z, int64_t M, int64_t N, int64_t K,
+                                     int64_t N2, coda_dtype dtype, int64_t head_dim, int64_t rope_cols, double base,
+                                     int64_t seq_len, const int32_t* positions, void* workspace,
+                                     cudaStream_t stream) {
+  coda::GemmProblem p;
+  TRY(block_prepare(coda::kEpiRowScale, X, W1t, R, W2t, nullptr, eps, H, P, r_out, Z, M, N, K, N2, dtype, workspace,
+                    stream, &p));
+  const RopeArgs rope = {head_dim, rope_cols, base, seq_len, positions};
+  TRY(check_rope(&rope, M, N2, dtype));
+  if (p.M == 0) return CODA_OK;
+  const int ob = out_bytes(dtype);
+  const int64_t T = coda_partial_cols(N);
+  const Range outs[] = {rng("H", H, M * N * ob), rng("P", P, M * T * 4), rng("r_out", r_out, r_out ? M * 4 : 0),
+                        rng("Z", Z, M * N2 * ob), rng("workspace", workspace, coda_block_workspace_bytes(M))};
+  const Range ins[] = {rng("positions", positions, positions ? M * 4 : 0)};
+  TRY(check_overlaps(outs, 5, ins, 1));
+  set_rope(p.b.ep, &rope);
+  return run_gemm(dtype, p);
 }
 
 coda_status coda_block_swiglu(const void* X, const void* W1t, const void* R, const void* Wgt, const void* Wut,

@@ -301,6 +301,18 @@ CODA_API coda_status coda_block_rowscale_fp8(const void* A, const float* amax_a,
                                              int64_t M, int64_t N, int64_t K, int64_t N2, void* workspace,
                                              cudaStream_t stream);
 
+/* coda_block_rowscale with RoPE on the consuming GEMM's leading columns (the
+ * Q and K heads of a fused QKV weight), as coda_gemm_rowscale_rope does it:
+ * the LLaMA block tail's next-layer QKV projection, normalised, projected and
+ * rotated in the same launch as the down projection and its residual add.
+ * head_dim, rope_cols, base, seq_len and positions as for
+ * coda_gemm_rowscale_rope; the other arguments as for coda_block_rowscale. */
+CODA_API coda_status coda_block_rowscale_rope(const void* X, const void* W1t, const void* R, const void* W2t,
+                                              float eps, void* H, float* P, float* r_out, void* Z, int64_t M,
+                                              int64_t N, int64_t K, int64_t N2, coda_dtype dtype, int64_t head_dim,
+                                              int64_t rope_cols, double base, int64_t seq_len,
+                                              const int32_t* positions, void* workspace, cudaStream_t stream);
+
 /* coda_block_swiglu for callers that cannot allocate device memory (no
  * counterpart in the CODA write-ups: it exists for the way some programs
  * manage memory).  Runtimes that own all device memory and give a kernel

@@ -212,3 +212,19 @@ def test_fp8_blocks_check_their_arguments(lib):
     # the FP8 workspace holds three counters per 128-row band and two more
     assert lib.coda_block_fp8_workspace_bytes(1000) == (3 * 8 + 2) * 4
     assert lib.coda_block_fp8_workspace_bytes(-1) == -1
+
+
+def test_block_rope_checks_rope_arguments(lib):
+    """coda_block_rowscale_rope rejects RoPE arguments as coda_gemm_rowscale_rope
+    does, before anything is enqueued."""
+    def call(head_dim=64, rope_cols=256, base=500000.0, seq_len=128, positions=None, N2=384):
+        return lib.coda_block_rowscale_rope(A, A + 64 * MB, A + 128 * MB, A + 192 * MB, 1e-5, A + 256 * MB,
+                                            A + 320 * MB, None, A + 384 * MB, 256, 512, 512, N2, 1, head_dim,
+                                            rope_cols, base, seq_len, positions, A + 448 * MB, None)
+    assert call(head_dim=60) == g.CODA_ERR_INVALID_ARG           # bf16: a multiple of 8
+    assert call(rope_cols=448) == g.CODA_ERR_INVALID_ARG         # beyond N2
+    assert call(rope_cols=96) == g.CODA_ERR_INVALID_ARG          # not a multiple of head_dim
+    assert call(base=1.0) == g.CODA_ERR_INVALID_ARG
+    assert call(seq_len=0) == g.CODA_ERR_INVALID_ARG             # no positions and no sequence length
+    assert call(positions=A + 256 * MB) == g.CODA_ERR_INVALID_ARG  # positions inside the output H
+    assert b"overlaps" in lib.coda_last_error()
