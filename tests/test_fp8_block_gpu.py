@@ -11,7 +11,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 from coda_inputs import WORKLOADS, Workload, make_inputs
 from parity_util import compare, oracle_ref, to_device
 

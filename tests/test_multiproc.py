@@ -26,7 +26,6 @@ def test_reference_arm_under_torchrun_two_ranks():
 
 
 def _rank_main(rank, port, out):
-    import torch.distributed as dist
     sys.path.insert(0, ROOT)
     import bench
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE="2")
