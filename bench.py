@@ -1089,7 +1089,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["coda", "reference", "unfused"], default="coda")
     ap.add_argument("--workload", default="llama8b_chain",
-                    choices=["llama1b_attn_out_swiglu", "llama1b_mlp_down_qkv", "llama8b_chain", "llama8b_chain_fp8"],
+                    choices=["llama1b_attn_out_swiglu", "llama1b_mlp_down_qkv", "llama8b_chain", "llama8b_chain_fp8",
+                             "llama70b_chain"],
                     help="the default is the largest bf16 configuration (the LLaMA-3-8B chain); the others "
                          "are for the per-configuration tables")
     ap.add_argument("--reduce", choices=["auto", "block", "fused", "separate"], default="auto",

@@ -63,8 +63,9 @@ class Workload:
         return dataclasses.replace(self, M=M)
 
 
-# The five workloads: tiny fp32 block; LLaMA-3-1B attention-out + gate/up;
-# LLaMA-3-1B MLP-down + QKV; LLaMA-3-8B full chain (bf16); the same in FP8.
+# The workloads: tiny fp32 block; LLaMA-3-1B attention-out + gate/up;
+# LLaMA-3-1B MLP-down + QKV; LLaMA-3-8B full chain (bf16); the same in FP8;
+# and the full chain at LLaMA-3-70B shapes.
 WORKLOADS: Dict[str, Workload] = {
     "tiny_f32": Workload("tiny_f32", "rowscale", 256, 512, 512, 512, 0, "f32", 1e-6, 0),
     "llama1b_attn_out_swiglu": Workload("llama1b_attn_out_swiglu", "swiglu", 8192, 2048, 2048, 8192, 0,
@@ -74,6 +75,10 @@ WORKLOADS: Dict[str, Workload] = {
     "llama8b_chain": Workload("llama8b_chain", "full", 16384, 4096, 4096, 6144, 14336, "bf16", 1e-5, 2),
     "llama8b_chain_fp8": Workload("llama8b_chain_fp8", "full", 32768, 4096, 4096, 6144, 14336, "e4m3",
                                   1e-5, 3, heavy_rows=0.05),
+    # the write-up's largest hidden size: LLaMA-3-70B shapes (hidden 8192,
+    # intermediate 28672, QKV 64 query + 2 x 8 key/value heads of 128 = 10240),
+    # the same 16384 tokens and distributions as the 8B chain
+    "llama70b_chain": Workload("llama70b_chain", "full", 16384, 8192, 8192, 10240, 28672, "bf16", 1e-5, 4),
 }
 
 

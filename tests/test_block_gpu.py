@@ -84,14 +84,16 @@ def test_block_full_size_equals_separate_calls(name):
     assert torch.count_nonzero(ws).item() == 0
 
 
-def test_block_full_size_8b_chain_equals_separate_calls():
+@pytest.mark.parametrize("name", ["llama8b_chain", "llama70b_chain"])
+def test_block_full_size_chain_equals_separate_calls(name):
     """The LLaMA-8B block-tail chain as two one-launch blocks (Wo + gate/up,
-    then down + QKV, the bench's default step), at full size.  The second block
-    has phase-A tiles of K = 14336 against phase-B tiles of K = 4096 and 1024
-    phase-A tiles over 76 CTA pairs, so its units walk the balanced order."""
+    then down + QKV, the bench's default step), at full size, and the same at
+    LLaMA-70B shapes.  The second 8B block has phase-A tiles of K = 14336
+    against phase-B tiles of K = 4096 and 1024 phase-A tiles over 76 CTA pairs,
+    so its units walk the balanced order."""
     import gemm_epilogue_fusion_gb300 as g
     from gemm_epilogue_fusion_gb300 import chain as C
-    w = WORKLOADS["llama8b_chain"]
+    w = WORKLOADS[name]
     inp = make_inputs(w)
     d = to_device(inp)
     sep = run_gpu(w, d, fused_reduce=True)

@@ -77,12 +77,13 @@ def test_llama8b_chain_small_m():
     _check(WORKLOADS["llama8b_chain"].with_rows(130))
 
 
-@pytest.mark.parametrize("name", ["llama1b_attn_out_swiglu", "llama1b_mlp_down_qkv", "llama8b_chain"])
+@pytest.mark.parametrize("name", ["llama1b_attn_out_swiglu", "llama1b_mlp_down_qkv", "llama8b_chain",
+                                  "llama70b_chain"])
 def test_full_size_sampled_rows(name):
     """Full workload size, the launch configuration the benchmark times;
     the oracle checks a seeded sample of rows including the first and last."""
     w = WORKLOADS[name]
-    rows = sample_rows(w.M, 12 if name == "llama8b_chain" else 24)
+    rows = sample_rows(w.M, 12 if w.chain == "full" else 24)
     errs = _check(w, rows)
     print(name, errs)
 
