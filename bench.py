@@ -691,7 +691,7 @@ def run_coda(args, w):
     # ---- end to end: pinned host X, R in and the block's outputs out, every
     # step.  Two buffer slots and three streams, so one step's copies overlap
     # the compute of its neighbours (copy engines and SMs work concurrently).
-    e2e_steps = max(20, min(200, args.steps // 5))
+    e2e_steps = max(40, min(200, args.steps // 2))
     outs = E2E_OUT[w.chain]
     s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     slots = []
