@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cinttypes>
 #include <climits>
 #include <cmath>
@@ -93,6 +94,17 @@ coda_status check_scalar_ptr(const void* p, const char* name) {
     if (s_ != CODA_OK) return s_;        \
   } while (0)
 
+// Byte extents of every operand of an M x N x K product must fit int64, and
+// the kernels' tile indices are 32-bit: bound both at the smallest tile,
+// 128 x 128 outputs.  M, N, K are already within [0, 2^31).
+coda_status check_extents(int64_t M, int64_t N, int64_t K, const char* nname) {
+  REQUIRE(M * N < (int64_t(1) << 60) && M * K < (int64_t(1) << 60) && N * K < (int64_t(1) << 60),
+          "M = %" PRId64 ", %s = %" PRId64 ", K = %" PRId64 ": a matrix of 2^60 elements or more", M, nname, N, K);
+  REQUIRE(((M + 127) / 128) * ((N + 127) / 128) < INT32_MAX / 2,
+          "M = %" PRId64 ", %s = %" PRId64 ": too many output tiles for the kernels' 32-bit tile indices", M, nname, N);
+  return CODA_OK;
+}
+
 // Shape rules common to the GEMM calls.
 coda_status check_gemm_dims(int64_t M, int64_t N, int64_t K, coda_dtype dt, const char* nname) {
   REQUIRE(valid_dtype(dt), "unknown dtype %d", static_cast<int>(dt));
@@ -103,13 +115,7 @@ coda_status check_gemm_dims(int64_t M, int64_t N, int64_t K, coda_dtype dt, cons
           16 / elem_bytes(dt));
   REQUIRE((N * out_bytes(dt)) % 16 == 0, "%s = %" PRId64 " must be a multiple of %d for this dtype (16-byte rows)",
           nname, N, 16 / out_bytes(dt));
-  // byte extents of every operand must fit int64, and the kernels' tile
-  // indices are 32-bit: bound both at the smallest tile, 128 x 128 outputs
-  REQUIRE(M * N < (int64_t(1) << 60) && M * K < (int64_t(1) << 60) && N * K < (int64_t(1) << 60),
-          "M = %" PRId64 ", %s = %" PRId64 ", K = %" PRId64 ": a matrix of 2^60 elements or more", M, nname, N, K);
-  REQUIRE(((M + 127) / 128) * ((N + 127) / 128) < INT32_MAX / 2,
-          "M = %" PRId64 ", %s = %" PRId64 ": too many output tiles for the kernels' 32-bit tile indices", M, nname, N);
-  return CODA_OK;
+  return check_extents(M, N, K, nname);
 }
 
 coda_status check_scales(coda_dtype dt, const float* a, const char* an, const float* b, const char* bn,
@@ -155,13 +161,17 @@ coda_status zero_scalar(float* p, cudaStream_t s) {
 namespace coda {
 
 int device_sm_count() {
-  static int cached[64] = {0};
+  // host threads may ask at once: each slot is written with the same value
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-  if (dev < 64) cached[dev] = n;
+  if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -255,7 +265,8 @@ coda_status coda_fold_gamma(const void* Wt, const float* gamma, void* Wt_out, in
                             coda_dtype dtype, cudaStream_t stream) {
   g_msg[0] = 0;
   REQUIRE(dtype == CODA_F32 || dtype == CODA_BF16, "coda_fold_gamma: dtype must be CODA_F32 or CODA_BF16");
-  REQUIRE(N_out >= 0 && K > 0 && N_out < INT32_MAX && K < INT32_MAX, "coda_fold_gamma: bad shape");
+  REQUIRE(N_out >= 0 && K > 0 && N_out < INT32_MAX && K < INT32_MAX && N_out * K < (int64_t(1) << 60),
+          "coda_fold_gamma: bad shape");
   REQUIRE((K * elem_bytes(dtype)) % 16 == 0, "coda_fold_gamma: K must give 16-byte rows");
   if (N_out == 0) return CODA_OK;
   TRY(check_ptr(Wt, "Wt"));
@@ -538,6 +549,7 @@ coda_status coda_gemm(const void* A, coda_layout a_layout, const void* B, coda_l
   REQUIRE(!(a_mn || b_mn) || dtype == CODA_BF16, "MN-major operands are bf16 only");
   REQUIRE(!(a_mn && !b_mn), "an MN-major A needs an MN-major B");
   REQUIRE(M >= 0 && M < INT32_MAX && N > 0 && N < INT32_MAX && K > 0 && K < INT32_MAX, "bad shape");
+  TRY(check_extents(M, N, K, "N"));
   const int eb = elem_bytes(dtype), ob = out_bytes(dtype);
   REQUIRE(((a_mn ? M : K) * eb) % 16 == 0, "A's rows must be a multiple of 16 bytes");
   REQUIRE(((b_mn ? N : K) * eb) % 16 == 0, "B's rows must be a multiple of 16 bytes");
@@ -614,8 +626,8 @@ coda_status coda_rmsnorm_backward(const void* dY, const void* H, const float* r,
                                   const void* dH_in, void* dH, void* Yt, float* dgamma, float* workspace, int64_t M,
                                   int64_t N, cudaStream_t stream) {
   g_msg[0] = 0;
-  REQUIRE(M >= 0 && M < INT32_MAX && N > 0 && N < INT32_MAX && N % 8 == 0,
-          "coda_rmsnorm_backward: M in [0, 2^31), N a positive multiple of 8");
+  REQUIRE(M >= 0 && M < INT32_MAX && N > 0 && N < INT32_MAX && N % 8 == 0 && M * N < (int64_t(1) << 60),
+          "coda_rmsnorm_backward: M in [0, 2^31), N a positive multiple of 8, M N below 2^60");
   if (M == 0) {
     TRY(check_scalar_ptr(dgamma, "dgamma"));
     cudaError_t e = cudaMemsetAsync(dgamma, 0, static_cast<size_t>(N) * sizeof(float), stream);
@@ -981,7 +993,7 @@ coda_status coda_block_rowscale_fp8(const void* X, const float* amax_x, uint8_t*
 coda_status coda_amax(const void* x, int64_t n, coda_dtype dtype, float* amax, cudaStream_t stream) {
   g_msg[0] = 0;
   REQUIRE(dtype == CODA_F32 || dtype == CODA_BF16, "coda_amax: dtype must be CODA_F32 or CODA_BF16");
-  REQUIRE(n >= 0, "coda_amax: n < 0");
+  REQUIRE(n >= 0 && n < (int64_t(1) << 60), "coda_amax: n out of range [0, 2^60)");
   TRY(check_scalar_ptr(amax, "amax"));
   TRY(zero_scalar(amax, stream));
   if (n == 0) return CODA_OK;
@@ -997,7 +1009,7 @@ coda_status coda_quantize_e4m3(const void* x, int64_t n, coda_dtype dtype, const
                                float* scale, cudaStream_t stream) {
   g_msg[0] = 0;
   REQUIRE(dtype == CODA_F32 || dtype == CODA_BF16, "coda_quantize_e4m3: dtype must be CODA_F32 or CODA_BF16");
-  REQUIRE(n >= 0, "coda_quantize_e4m3: n < 0");
+  REQUIRE(n >= 0 && n < (int64_t(1) << 60), "coda_quantize_e4m3: n out of range [0, 2^60)");
   TRY(check_scalar_ptr(amax, "amax"));
   TRY(check_scalar_ptr(scale, "scale"));
   if (n > 0) {

@@ -77,6 +77,23 @@ def test_rejects_sizes_beyond_32_bit_tile_indices(lib):
     assert b"tile" in lib.coda_last_error()
 
 
+def test_every_call_bounds_its_extents(lib):
+    # sizes whose byte extents would overflow int64 are refused by every call
+    # that takes them, before anything is enqueued (the addresses are fake)
+    big = (1 << 31) - 8
+    B, D = A + 64 * MB, A + 128 * MB
+    assert lib.coda_gemm(A, 0, B, 1, D, big, big, 8, 1, None, None, None) == g.CODA_ERR_INVALID_ARG
+    assert b"2^60" in lib.coda_last_error()
+    assert lib.coda_gemm(A, 1, B, 1, D, 1 << 30, 1 << 20, 8, 1, None, None, None) == g.CODA_ERR_INVALID_ARG
+    assert b"tile" in lib.coda_last_error()
+    assert lib.coda_fold_gamma(A, B, D, big, big - 7, 1, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_rmsnorm_backward(A, B, A + 128 * MB, A + 129 * MB, A + 130 * MB, None, A + 192 * MB,
+                                     A + 256 * MB, A + 320 * MB, A + 321 * MB, big, big - 7, None) \
+        == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_amax(A, 1 << 61, 1, B, None) == g.CODA_ERR_INVALID_ARG
+    assert lib.coda_quantize_e4m3(A, 1 << 61, 1, B, D, B + 4, None) == g.CODA_ERR_INVALID_ARG
+
+
 def test_rejects_overlapping_outputs(lib):
     assert _rpr(lib, H=A + 128 * MB) == g.CODA_ERR_INVALID_ARG   # h over R
     assert b"overlaps input R" in lib.coda_last_error()
