@@ -129,8 +129,78 @@ def _out_dtype(code: int) -> torch.dtype:
     return torch.float32 if code == CODA_F32 else torch.bfloat16
 
 
+_F32 = (torch.float32,)
+_BYTE = (torch.uint8, torch.float8_e4m3fn)
+
+
+def _want(t: Optional[torch.Tensor], name: str, shape=None, dtypes=None, numel=None, nbytes=None):
+    """Checks that a given tensor matches the sizes the call passes to the
+    library (the kernels read and write exactly those extents): its shape,
+    its dtype, at least `numel` elements (scalars) or `nbytes` bytes
+    (workspaces).  None passes (a NULL argument, which the library checks)."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {' or '.join(str(d) for d in dtypes)}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, expected at least {numel}")
+    if nbytes is not None and t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, expected at least {nbytes}")
+
+
+def _operand_dtypes(code: int):
+    return {CODA_F32: (torch.float32,), CODA_BF16: (torch.bfloat16,), CODA_E4M3: _BYTE}[code]
+
+
+def _want_scalars(**scalars):
+    """Per-tensor scales and amax outputs: one fp32 each."""
+    for name, t in scalars.items():
+        _want(t, name, dtypes=_F32, numel=1)
+
+
+def _want_block(X, W1t, R, Wb, Wb2, H, P, out, r_out, workspace, n_out, code, out_name, wb_name):
+    """The tensors of a one-launch block: X [M, K], W1t [N, K], R and h [M, N],
+    the consumer's weights [n_out, N], P [M, T], the output [M, n_out]."""
+    M, K = X.shape
+    N = W1t.shape[0]
+    ops, od = _operand_dtypes(code), (_out_dtype(code),)
+    _want(W1t, "W1t", (N, K), ops)
+    _want(R, "R", (M, N), od)
+    _want(Wb, wb_name, (n_out, N), ops)
+    _want(Wb2, "Wut", (n_out, N), ops)
+    _want(H, "H", (M, N), od)
+    _want(P, "P", (M, coda_partial_cols(N)), _F32)
+    _want(out, out_name, (M, n_out), od)
+    _want(r_out, "r_out", (M,), _F32)
+    _want(workspace, "workspace", nbytes=coda_block_workspace_bytes(M))
+
+
+def _want_fp8_block(A, amax_a, Aq, scale_a, W1t, scale_w1, R, Wb, scale_wb, Wb2, scale_wb2, H, P, r_out, amax_h, Hq,
+                    scale_h, out, amax_out, workspace, M, N, K, n_out, out_name, wb_name):
+    """The tensors of an FP8 one-launch block (e4m3 operands as uint8 bytes)."""
+    bf = (torch.bfloat16,)
+    _want(A, "A", (M, K), bf)
+    _want(Aq, "Aq", (M, K), _BYTE)
+    _want(W1t, "W1t", (N, K), _BYTE)
+    _want(R, "R", (M, N), bf)
+    _want(Wb, wb_name, (n_out, N), _BYTE)
+    _want(Wb2, "Wut", (n_out, N), _BYTE)
+    _want(H, "H", (M, N), bf)
+    _want(P, "P", (M, coda_partial_cols(N)), _F32)
+    _want(r_out, "r_out", (M,), _F32)
+    _want(Hq, "Hq", (M, N), _BYTE)
+    _want(out, out_name, (M, n_out), bf)
+    _want_scalars(amax_a=amax_a, scale_a=scale_a, scale_w1=scale_w1, scale_w=scale_wb, scale_wu=scale_wb2,
+                  amax_h=amax_h, scale_h=scale_h, amax_act=amax_out)
+    _want(workspace, "workspace", nbytes=coda_block_fp8_workspace_bytes(M))
+
+
 def _dev(t: Optional[torch.Tensor], name: str):
-    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    """Device pointer of a contiguous CUDA tensor on the current device (None -> NULL)."""
     if t is None:
         return None
     if not isinstance(t, torch.Tensor):
@@ -139,6 +209,9 @@ def _dev(t: Optional[torch.Tensor], name: str):
         raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if t.device.index is not None and t.device.index != torch.cuda.current_device():
+        # the library launches on the current device
+        raise ValueError(f"{name} is on {t.device} but the current device is cuda:{torch.cuda.current_device()}")
     return t.data_ptr() or None
 
 
@@ -157,6 +230,9 @@ def coda_fold_gamma(Wt: torch.Tensor, gamma: torch.Tensor, out: Optional[torch.T
     lib = load_library()
     N_out, K = Wt.shape
     out = torch.empty_like(Wt) if out is None else out
+    _want(Wt, "Wt", dtypes=(torch.float32, torch.bfloat16))
+    _want(gamma, "gamma", (K,), _F32)
+    _want(out, "out", (N_out, K), (Wt.dtype,))
     _check(lib.coda_fold_gamma(_dev(Wt, "Wt"), _dev(gamma, "gamma"), _dev(out, "out"), N_out, K, _dtype_code(Wt),
                                _stream(Wt, stream)))
     return out
@@ -173,6 +249,12 @@ def coda_gemm_residual_partial_rms(X, W1t, R, H=None, P=None, *, scale_x=None, s
         H = torch.empty(M, N, dtype=_out_dtype(code), device=X.device)
     if P is None:
         P = torch.empty(M, max(coda_partial_cols(N), 0), dtype=torch.float32, device=X.device)
+    ops, od = _operand_dtypes(code), (_out_dtype(code),)
+    _want(W1t, "W1t", (N, K), ops)
+    _want(R, "R", (M, N), od)
+    _want(H, "H", (M, N), od)
+    _want(P, "P", (M, coda_partial_cols(N)), _F32)
+    _want_scalars(scale_x=scale_x, scale_w=scale_w, amax_h=amax_h)
     _check(lib.coda_gemm_residual_partial_rms(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(H, "H"),
                                               _dev(P, "P"), M, N, K, code, _dev(scale_x, "scale_x"),
                                               _dev(scale_w, "scale_w"), _dev(amax_h, "amax_h"), _stream(X, stream)))
@@ -185,6 +267,8 @@ def coda_rms_reduce(P, N: int, eps: float, r=None, stream=None):
     M = P.shape[0]
     if r is None:
         r = torch.empty(M, dtype=torch.float32, device=P.device)
+    _want(P, "P", (M, coda_partial_cols(N)), _F32)
+    _want(r, "r", (M,), _F32)
     _check(lib.coda_rms_reduce(_dev(P, "P"), M, N, float(eps), _dev(r, "r"), _stream(P, stream)))
     return r
 
@@ -197,6 +281,10 @@ def coda_gemm_rowscale(H, W2t, r, Z=None, *, scale_h=None, scale_w=None, stream=
     code = _dtype_code(H)
     if Z is None:
         Z = torch.empty(M, N2, dtype=_out_dtype(code), device=H.device)
+    _want(W2t, "W2t", (N2, K), _operand_dtypes(code))
+    _want(r, "r", (M,), _F32)
+    _want(Z, "Z", (M, N2), (_out_dtype(code),))
+    _want_scalars(scale_h=scale_h, scale_w=scale_w)
     _check(lib.coda_gemm_rowscale(_dev(H, "H"), _dev(W2t, "W2t"), _dev(r, "r"), _dev(Z, "Z"), M, N2, K, code,
                                   _dev(scale_h, "scale_h"), _dev(scale_w, "scale_w"), _stream(H, stream)))
     return Z
@@ -211,6 +299,11 @@ def coda_gemm_swiglu(H, Wgt, Wut, r=None, Act=None, *, scale_h=None, scale_wg=No
     code = _dtype_code(H)
     if Act is None:
         Act = torch.empty(M, I, dtype=_out_dtype(code), device=H.device)
+    _want(Wgt, "Wgt", (I, K), _operand_dtypes(code))
+    _want(Wut, "Wut", (I, K), _operand_dtypes(code))
+    _want(r, "r", (M,), _F32)
+    _want(Act, "Act", (M, I), (_out_dtype(code),))
+    _want_scalars(scale_h=scale_h, scale_wg=scale_wg, scale_wu=scale_wu, amax_act=amax_act)
     _check(lib.coda_gemm_swiglu(_dev(H, "H"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"), _dev(r, "r"), _dev(Act, "Act"),
                                 M, I, K, code, _dev(scale_h, "scale_h"), _dev(scale_wg, "scale_wg"),
                                 _dev(scale_wu, "scale_wu"), _dev(amax_act, "amax_act"), _stream(H, stream)))
@@ -226,6 +319,11 @@ def coda_gemm_rowscale_fused_rms(H, W2t, P, eps: float, Z=None, r_out=None, *, s
     code = _dtype_code(H)
     if Z is None:
         Z = torch.empty(M, N2, dtype=_out_dtype(code), device=H.device)
+    _want(W2t, "W2t", (N2, K), _operand_dtypes(code))
+    _want(P, "P", (M, coda_partial_cols(K)), _F32)
+    _want(r_out, "r_out", (M,), _F32)
+    _want(Z, "Z", (M, N2), (_out_dtype(code),))
+    _want_scalars(scale_h=scale_h, scale_w=scale_w)
     _check(lib.coda_gemm_rowscale_fused_rms(_dev(H, "H"), _dev(W2t, "W2t"), _dev(P, "P"), float(eps),
                                             _dev(r_out, "r_out"), _dev(Z, "Z"), M, N2, K, code,
                                             _dev(scale_h, "scale_h"), _dev(scale_w, "scale_w"), _stream(H, stream)))
@@ -241,6 +339,12 @@ def coda_gemm_swiglu_fused_rms(H, Wgt, Wut, P, eps: float, Act=None, r_out=None,
     code = _dtype_code(H)
     if Act is None:
         Act = torch.empty(M, I, dtype=_out_dtype(code), device=H.device)
+    _want(Wgt, "Wgt", (I, K), _operand_dtypes(code))
+    _want(Wut, "Wut", (I, K), _operand_dtypes(code))
+    _want(P, "P", (M, coda_partial_cols(K)), _F32)
+    _want(r_out, "r_out", (M,), _F32)
+    _want(Act, "Act", (M, I), (_out_dtype(code),))
+    _want_scalars(scale_h=scale_h, scale_wg=scale_wg, scale_wu=scale_wu, amax_act=amax_act)
     _check(lib.coda_gemm_swiglu_fused_rms(_dev(H, "H"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"), _dev(P, "P"),
                                           float(eps), _dev(r_out, "r_out"), _dev(Act, "Act"), M, I, K, code,
                                           _dev(scale_h, "scale_h"), _dev(scale_wg, "scale_wg"),
@@ -260,6 +364,13 @@ def coda_gemm_rowscale_rope(H, W2t, head_dim: int, rope_cols: int, base: float, 
     code = _dtype_code(H)
     if Z is None:
         Z = torch.empty(M, N2, dtype=_out_dtype(code), device=H.device)
+    _want(W2t, "W2t", (N2, K), _operand_dtypes(code))
+    _want(r, "r", (M,), _F32)
+    _want(P, "P", (M, coda_partial_cols(K)), _F32)
+    _want(r_out, "r_out", (M,), _F32)
+    _want(Z, "Z", (M, N2), (_out_dtype(code),))
+    _want(positions, "positions", (M,), (torch.int32,))
+    _want_scalars(scale_h=scale_h, scale_w=scale_w)
     _check(lib.coda_gemm_rowscale_rope(_dev(H, "H"), _dev(W2t, "W2t"), _dev(r, "r"), _dev(P, "P"), float(eps),
                                        _dev(r_out, "r_out"), _dev(Z, "Z"), M, N2, K, code, _dev(scale_h, "scale_h"),
                                        _dev(scale_w, "scale_w"), head_dim, rope_cols, float(base), seq_len,
@@ -279,6 +390,10 @@ def coda_gemm(A, B, *, a_mn: bool = False, b_mn: bool = False, row_scale=None, c
     code = _dtype_code(A)
     if D is None:
         D = torch.empty(M, N, dtype=_out_dtype(code), device=A.device)
+    _want(B, "B", dtypes=(A.dtype,))
+    _want(D, "D", (M, N), (_out_dtype(code),))
+    _want(row_scale, "row_scale", (M,), _F32)
+    _want(col_scale, "col_scale", (N,), _F32)
     _check(lib.coda_gemm(_dev(A, "A"), int(a_mn), _dev(B, "B"), int(b_mn), _dev(D, "D"), M, N, K, code,
                          _dev(row_scale, "row_scale"), _dev(col_scale, "col_scale"), _stream(A, stream)))
     return D
@@ -293,6 +408,13 @@ def coda_gemm_grad_norm(dOut, Wt, H, gamma, dY=None, S=None, stream=None):
         dY = torch.empty(M, N, dtype=torch.bfloat16, device=dOut.device)
     if S is None:
         S = torch.empty(M, coda_partial_cols(N), dtype=torch.float32, device=dOut.device)
+    bf = (torch.bfloat16,)
+    _want(dOut, "dOut", dtypes=bf)
+    _want(Wt, "Wt", (K, N), bf)
+    _want(H, "H", (M, N), bf)
+    _want(gamma, "gamma", (N,), _F32)
+    _want(dY, "dY", (M, N), bf)
+    _want(S, "S", (M, coda_partial_cols(N)), _F32)
     _check(lib.coda_gemm_grad_norm(_dev(dOut, "dOut"), _dev(Wt, "Wt"), _dev(H, "H"), _dev(gamma, "gamma"),
                                    _dev(dY, "dY"), _dev(S, "S"), M, N, K, _dtype_code(dOut), _stream(dOut, stream)))
     return dY, S
@@ -310,6 +432,14 @@ def coda_rmsnorm_backward(dY, H, r, gamma, S, dH_in=None, dH=None, Yt=None, dgam
     if workspace is None:
         n = lib.coda_rmsnorm_backward_workspace_bytes(M, N)
         workspace = torch.empty(max(n // 4, 1), dtype=torch.float32, device=dY.device)
+    bf = (torch.bfloat16,)
+    for t, name in ((dY, "dY"), (H, "H"), (dH_in, "dH_in"), (dH, "dH"), (Yt, "Yt")):
+        _want(t, name, (M, N), bf)
+    _want(r, "r", (M,), _F32)
+    _want(gamma, "gamma", (N,), _F32)
+    _want(S, "S", (M, coda_partial_cols(N)), _F32)
+    _want(dgamma, "dgamma", (N,), _F32)
+    _want(workspace, "workspace", nbytes=lib.coda_rmsnorm_backward_workspace_bytes(M, N))
     _check(lib.coda_rmsnorm_backward(_dev(dY, "dY"), _dev(H, "H"), _dev(r, "r"), _dev(gamma, "gamma"), _dev(S, "S"),
                                      _dev(dH_in, "dH_in"), _dev(dH, "dH"), _dev(Yt, "Yt"), _dev(dgamma, "dgamma"),
                                      _dev(workspace, "workspace"), M, N, _stream(dY, stream)))
@@ -326,6 +456,15 @@ def coda_gemm_swiglu_save(H, Wgt, Wut, *, r=None, P=None, eps: float = 0.0, r_ou
         Act = torch.empty(M, I, dtype=torch.bfloat16, device=H.device)
     if GU is None:
         GU = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=H.device)
+    bf = (torch.bfloat16,)
+    _want(H, "H", dtypes=bf)
+    _want(Wgt, "Wgt", (I, K), bf)
+    _want(Wut, "Wut", (I, K), bf)
+    _want(r, "r", (M,), _F32)
+    _want(P, "P", (M, coda_partial_cols(K)), _F32)
+    _want(r_out, "r_out", (M,), _F32)
+    _want(Act, "Act", (M, I), bf)
+    _want(GU, "GU", (M, 2 * I), bf)
     _check(lib.coda_gemm_swiglu_save(_dev(H, "H"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"), _dev(r, "r"), _dev(P, "P"),
                                      float(eps), _dev(r_out, "r_out"), _dev(Act, "Act"), _dev(GU, "GU"), M, I, K,
                                      _dtype_code(H), _stream(H, stream)))
@@ -339,6 +478,11 @@ def coda_gemm_swiglu_backward(dOut, Wt, GU, dGU=None, stream=None):
     I = Wt.shape[1]
     if dGU is None:
         dGU = torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dOut.device)
+    bf = (torch.bfloat16,)
+    _want(dOut, "dOut", dtypes=bf)
+    _want(Wt, "Wt", (K, I), bf)
+    _want(GU, "GU", (M, 2 * I), bf)
+    _want(dGU, "dGU", (M, 2 * I), bf)
     _check(lib.coda_gemm_swiglu_backward(_dev(dOut, "dOut"), _dev(Wt, "Wt"), _dev(GU, "GU"), _dev(dGU, "dGU"), M, I,
                                          K, _dtype_code(dOut), _stream(dOut, stream)))
     return dGU
@@ -372,6 +516,7 @@ def coda_block_rowscale(X, W1t, R, W2t, eps: float, workspace, H=None, P=None, Z
     N, N2 = W1t.shape[0], W2t.shape[0]
     code = _dtype_code(X)
     H, P, Z = _block_outputs(X, R, N, N2, H, P, Z, code)
+    _want_block(X, W1t, R, W2t, None, H, P, Z, r_out, workspace, N2, code, "Z", "W2t")
     _check(lib.coda_block_rowscale(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(W2t, "W2t"), float(eps),
                                    _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"), _dev(Z, "Z"), M, N, K, N2, code,
                                    _dev(workspace, "workspace"), _stream(X, stream)))
@@ -387,6 +532,8 @@ def coda_block_rowscale_rope(X, W1t, R, W2t, eps: float, workspace, head_dim: in
     N, N2 = W1t.shape[0], W2t.shape[0]
     code = _dtype_code(X)
     H, P, Z = _block_outputs(X, R, N, N2, H, P, Z, code)
+    _want_block(X, W1t, R, W2t, None, H, P, Z, r_out, workspace, N2, code, "Z", "W2t")
+    _want(positions, "positions", (M,), (torch.int32,))
     _check(lib.coda_block_rowscale_rope(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(W2t, "W2t"), float(eps),
                                         _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"), _dev(Z, "Z"), M, N, K, N2,
                                         code, head_dim, rope_cols, float(base), seq_len, _dev(positions, "positions"),
@@ -402,6 +549,7 @@ def coda_block_swiglu(X, W1t, R, Wgt, Wut, eps: float, workspace, H=None, P=None
     N, I = W1t.shape[0], Wgt.shape[0]
     code = _dtype_code(X)
     H, P, Act = _block_outputs(X, R, N, I, H, P, Act, code)
+    _want_block(X, W1t, R, Wgt, Wut, H, P, Act, r_out, workspace, I, code, "Act", "Wgt")
     _check(lib.coda_block_swiglu(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(Wgt, "Wgt"), _dev(Wut, "Wut"),
                                  float(eps), _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"), _dev(Act, "Act"), M, N,
                                  K, I, code, _dev(workspace, "workspace"), _stream(X, stream)))
@@ -417,6 +565,7 @@ def coda_block_swiglu_noalloc(X, W1t, R, Wgt, Wut, eps: float, H=None, P=None, A
     N, I = W1t.shape[0], Wgt.shape[0]
     code = _dtype_code(X)
     H, P, Act = _block_outputs(X, R, N, I, H, P, Act, code)
+    _want_block(X, W1t, R, Wgt, Wut, H, P, Act, r_out, None, I, code, "Act", "Wgt")
     _check(lib.coda_block_swiglu_noalloc(_dev(X, "X"), _dev(W1t, "W1t"), _dev(R, "R"), _dev(Wgt, "Wgt"),
                                          _dev(Wut, "Wut"), float(eps), _dev(H, "H"), _dev(P, "P"), _dev(r_out, "r_out"),
                                          _dev(Act, "Act"), M, N, K, I, code, _stream(X, stream)))
@@ -461,6 +610,8 @@ def coda_block_swiglu_fp8(A, amax_a, W1t, scale_w1, R, Wgt, scale_wg, Wut, scale
     dev = src.device
     Aq, scale_a, H, P, amax_h, Hq, scale_h, Act = _fp8_block_buffers(M, N, K, I, dev, A, Aq, scale_a, H, P, amax_h,
                                                                       Hq, scale_h, Act)
+    _want_fp8_block(A, amax_a, Aq, scale_a, W1t, scale_w1, R, Wgt, scale_wg, Wut, scale_wu, H, P, r_out, amax_h,
+                    Hq, scale_h, Act, amax_act, workspace, M, N, K, I, "Act", "Wgt")
     _check(lib.coda_block_swiglu_fp8(_dev(A, "A"), _dev(amax_a, "amax_a"), _dev(Aq, "Aq"), _dev(scale_a, "scale_a"),
                                      _dev(W1t, "W1t"), _dev(scale_w1, "scale_w1"), _dev(R, "R"), _dev(Wgt, "Wgt"),
                                      _dev(scale_wg, "scale_wg"), _dev(Wut, "Wut"), _dev(scale_wu, "scale_wu"),
@@ -485,6 +636,8 @@ def coda_block_rowscale_fp8(A, amax_a, W1t, scale_w1, R, W2t, scale_w2, eps: flo
     dev = src.device
     Aq, scale_a, H, P, amax_h, Hq, scale_h, Z = _fp8_block_buffers(M, N, K, N2, dev, A, Aq, scale_a, H, P, amax_h,
                                                                     Hq, scale_h, Z)
+    _want_fp8_block(A, amax_a, Aq, scale_a, W1t, scale_w1, R, W2t, scale_w2, None, None, H, P, r_out, amax_h,
+                    Hq, scale_h, Z, None, workspace, M, N, K, N2, "Z", "W2t")
     _check(lib.coda_block_rowscale_fp8(_dev(A, "A"), _dev(amax_a, "amax_a"), _dev(Aq, "Aq"), _dev(scale_a, "scale_a"),
                                        _dev(W1t, "W1t"), _dev(scale_w1, "scale_w1"), _dev(R, "R"), _dev(W2t, "W2t"),
                                        _dev(scale_w2, "scale_w2"), float(eps), _dev(H, "H"), _dev(P, "P"),
@@ -499,6 +652,8 @@ def coda_amax(x, amax=None, stream=None):
     lib = load_library()
     if amax is None:
         amax = torch.empty(1, dtype=torch.float32, device=x.device)
+    _want(x, "x", dtypes=(torch.float32, torch.bfloat16))
+    _want(amax, "amax", dtypes=_F32, numel=1)
     _check(lib.coda_amax(_dev(x, "x"), x.numel(), _dtype_code(x), _dev(amax, "amax"), _stream(x, stream)))
     return amax
 
@@ -510,6 +665,10 @@ def coda_quantize_e4m3(x, amax, q=None, scale=None, stream=None):
         q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
     if scale is None:
         scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    _want(x, "x", dtypes=(torch.float32, torch.bfloat16))
+    _want(amax, "amax", dtypes=_F32, numel=1)
+    _want(q, "q", dtypes=_BYTE, numel=x.numel())
+    _want(scale, "scale", dtypes=_F32, numel=1)
     _check(lib.coda_quantize_e4m3(_dev(x, "x"), x.numel(), _dtype_code(x), _dev(amax, "amax"), _dev(q, "q"),
                                   _dev(scale, "scale"), _stream(x, stream)))
     return q, scale

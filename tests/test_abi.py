@@ -128,8 +128,48 @@ def test_rms_reduce_and_helpers_validate(lib):
 def test_binding_fails_loudly_without_cuda_tensors():
     import torch
     X = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(8, 8, dtype=torch.bfloat16)
+    P = torch.zeros(4, 1)
     with pytest.raises(ValueError, match="CUDA tensor"):
-        g.coda_gemm_residual_partial_rms(X, X, X, X, X)
+        g.coda_gemm_residual_partial_rms(X, W, X, X, P)
+
+
+def test_binding_checks_shapes_and_dtypes_before_the_library_sees_a_pointer():
+    """The kernels read and write the extents the sizes imply, so a tensor of
+    another shape or dtype would be read or written out of bounds: the binding
+    refuses it (these checks run before the CUDA-tensor check, so CPU tensors
+    show them)."""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    M, K, N = 4, 16, 8
+    X, W, R = torch.zeros(M, K, dtype=bf), torch.zeros(N, K, dtype=bf), torch.zeros(M, N, dtype=bf)
+    P = torch.zeros(M, 1)
+    cases = [
+        (lambda: g.coda_gemm_residual_partial_rms(X, W, R[:, :4].contiguous()), ValueError, "R has shape"),
+        (lambda: g.coda_gemm_residual_partial_rms(X, W, R.float()), TypeError, "R has dtype"),
+        (lambda: g.coda_gemm_residual_partial_rms(X, W[:, :8].contiguous(), R), ValueError, "W1t has shape"),
+        (lambda: g.coda_gemm_residual_partial_rms(X, W, R, P=torch.zeros(M, 2)), ValueError, "P has shape"),
+        (lambda: g.coda_rms_reduce(P, N, 1e-5, r=torch.zeros(M + 1)), ValueError, "r has shape"),
+        (lambda: g.coda_gemm_rowscale(X, W, torch.zeros(M, dtype=bf)), TypeError, "r has dtype"),
+        (lambda: g.coda_gemm_swiglu(X, W, W[:4].contiguous()), ValueError, "Wut has shape"),
+        (lambda: g.coda_gemm(X, W, D=torch.zeros(M, N + 8, dtype=bf)), ValueError, "D has shape"),
+        (lambda: g.coda_gemm(X, W.float()), TypeError, "B has dtype"),
+        (lambda: g.coda_gemm_grad_norm(X, torch.zeros(K, N, dtype=bf), R, torch.zeros(N + 1)), ValueError,
+         "gamma has shape"),
+        (lambda: g.coda_gemm_swiglu_backward(X, torch.zeros(K, 64, dtype=bf), torch.zeros(M, 64, dtype=bf)),
+         ValueError, "GU has shape"),
+        (lambda: g.coda_block_swiglu(X, W, R, torch.zeros(64, N, dtype=bf), torch.zeros(64, N, dtype=bf), 1e-5,
+                                     torch.zeros(0, dtype=torch.int32)), ValueError, "workspace holds"),
+        (lambda: g.coda_block_rowscale(X, W, R, torch.zeros(64, N + 8, dtype=bf), 1e-5,
+                                       torch.zeros(8, dtype=torch.int32)), ValueError, "W2t has shape"),
+        (lambda: g.coda_quantize_e4m3(X, torch.zeros(1), q=torch.zeros(M * K - 1, dtype=torch.uint8)), ValueError,
+         "q has"),
+        (lambda: g.coda_amax(X, amax=torch.zeros(1, dtype=bf)), TypeError, "amax has dtype"),
+        (lambda: g.coda_fold_gamma(W, torch.zeros(K + 1)), ValueError, "gamma has shape"),
+    ]
+    for fn, exc, msg in cases:
+        with pytest.raises(exc, match=msg):
+            fn()
 
 
 def test_block_calls_validate(lib):
