@@ -19,6 +19,9 @@
 //          those boxes into the slot ring, so the epilogue reads them from
 //          shared memory and writes its result in place; in a two-phase launch
 //          it also hands the slots of the second phase's boxes to the epilogue
+//   7..10  FP8 one-launch blocks only: quantiser warps that write the e4m3
+//          copies of phase A's input and of h, band by band, for the TMA loads
+//          of the GEMMs that follow in the same launch
 //
 // Epilogue programs.  The CODA write-ups ("CODA: the treasure hidden in the
 // epilogue") apply the memory-bound neighbours of a GEMM while its product is
