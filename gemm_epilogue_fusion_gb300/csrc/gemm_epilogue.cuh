@@ -183,9 +183,20 @@ struct GemmCfg {
   static constexpr uint32_t IDESC = make_idesc(FMT, FMT, TILE_M, BN, A_MN, B_MN);
 };
 
-// Elements of one quantiser chunk: 32 lanes x 6 groups of 16 elements.
+// Elements of one pass of a quantiser warp: 32 lanes x 6 groups of 16.
 constexpr int kQuantGroups = 6;
-constexpr int64_t kQuantChunk = 32 * 16 * kQuantGroups;
+constexpr int64_t kQuantPass = 32 * 16 * kQuantGroups;
+// Passes per chunk, the unit that is fenced and counted into its band.  The
+// fence waits for the warp's stores to land; paid once per pass, it kept the
+// quantiser warps waiting for most of their time (an in-launch pass over the
+// 8B chain's act ran 4.6x slower than the standalone quantise kernel), so a
+// chunk of several passes pays it once.  8 measured fastest of 1, 2, 4, 8;
+// larger chunks make a band complete later.
+#ifndef CODA_QUANT_PASSES
+#define CODA_QUANT_PASSES 8
+#endif
+constexpr int kQuantPasses = CODA_QUANT_PASSES;
+constexpr int64_t kQuantChunk = kQuantPasses * kQuantPass;
 // Chunks per row band of band_rows rows and `cols` columns (the last band
 // counts as many, its chunks past row M being empty).
 __host__ __device__ inline int quant_chunks_per_band(int band_rows, int cols) {
@@ -193,20 +204,21 @@ __host__ __device__ inline int quant_chunks_per_band(int band_rows, int cols) {
 }
 
 // One quantiser warp's share of a bf16 [M, cols] tensor -> e4m3 bytes: chunk
-// j (band j / cpb) for j = w, w + nw, ...; each chunk's bytes are made
-// visible (to the TMA loads of other CTAs too) before its band's counter is
-// released.  Software-pipelined: the loads of the next chunk are in flight
-// while the current one is converted, stored and fenced.  cols is a multiple
+// j (band j / cpb) for j = w, w + nw, ..., pass by pass; each chunk's bytes
+// are made visible (to the TMA loads of other CTAs too) before its band's
+// counter is released.  Software-pipelined: the loads of the next pass are in
+// flight while the current one is converted and stored.  cols is a multiple
 // of 16, so a group of 16 elements never crosses a row band's end.  Returns
 // false if the launch was aborted.
 struct QuantChunk {
   int64_t e0, e_end, band;  // first element of this lane, end of its band, band
 };
-__device__ __forceinline__ QuantChunk quant_chunk(int64_t j, int cpb, int64_t band_elems, int64_t total) {
+// Pass p of chunk j.
+__device__ __forceinline__ QuantChunk quant_chunk(int64_t j, int p, int cpb, int64_t band_elems, int64_t total) {
   const int lane = threadIdx.x & 31;
   const int64_t b = j / cpb;
   const int64_t e_band = b * band_elems;
-  return {e_band + (j - b * cpb) * kQuantChunk + 16 * lane, min(e_band + band_elems, total), b};
+  return {e_band + (j - b * cpb) * kQuantChunk + p * kQuantPass + 16 * lane, min(e_band + band_elems, total), b};
 }
 // The bf16 source is read once: streaming loads (evict first), so the
 // stream does not push the GEMM's operand panels out of L2.
@@ -243,14 +255,20 @@ __device__ __forceinline__ bool quantize_bands(const __nv_bfloat16* __restrict__
   const int64_t n_chunks = static_cast<int64_t>((M + band_rows - 1) / band_rows) * cpb;
   if (w >= n_chunks) return true;
   uint4 cur[kQuantGroups][2], nxt[kQuantGroups][2];
-  QuantChunk c = quant_chunk(w, cpb, band_elems, total);
+  int64_t j = w;
+  int p = 0;
+  QuantChunk c = quant_chunk(j, 0, cpb, band_elems, total);
   quant_load(src, c, cur);
-  for (int64_t j = w; j < n_chunks; j += nw) {
+  for (;;) {
     if (*abort_flag) return false;
-    const bool more = j + nw < n_chunks;
+    // the next pass: of this chunk, else the first of this warp's next chunk
+    const bool last_pass = p == kQuantPasses - 1;
+    const int64_t jn = last_pass ? j + nw : j;
+    const int pn = last_pass ? 0 : p + 1;
+    const bool more = jn < n_chunks;  // always true before a chunk's last pass
     QuantChunk cn = c;
     if (more) {
-      cn = quant_chunk(j + nw, cpb, band_elems, total);
+      cn = quant_chunk(jn, pn, cpb, band_elems, total);
       quant_load(src, cn, nxt);
     }
 #pragma unroll
@@ -262,19 +280,22 @@ __device__ __forceinline__ bool quantize_bands(const __nv_bfloat16* __restrict__
         *reinterpret_cast<uint4*>(dst + e) = e4m3x16<FAST>(f, s, inv);
       }
     }
-    // the codes, then the band's counter: generic stores read by TMA loads
-    fence_proxy_async_global();
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) red_release_gpu_add(ready + c.band, 1u);
-    if (more) {
-#pragma unroll
-      for (int g = 0; g < kQuantGroups; ++g) {
-        cur[g][0] = nxt[g][0];
-        cur[g][1] = nxt[g][1];
-      }
-      c = cn;
+    if (last_pass) {
+      // the chunk's codes, then its band's counter: generic stores read by TMA loads
+      fence_proxy_async_global();
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) red_release_gpu_add(ready + c.band, 1u);
     }
+    if (!more) break;
+#pragma unroll
+    for (int g = 0; g < kQuantGroups; ++g) {
+      cur[g][0] = nxt[g][0];
+      cur[g][1] = nxt[g][1];
+    }
+    c = cn;
+    j = jn;
+    p = pn;
   }
   return true;
 }
