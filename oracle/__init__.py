@@ -25,7 +25,9 @@ in tests/golden/, numpy fp64 matmul on a C0-sized case, the reparameterisation
 identity, RMSNorm scale invariance, silu special values, the E4M3 codec
 against torch's float8_e4m3fn over all 256 codes, a hand-derived FP8 chain in
 which every quantisation site (and the fold before it) changes the result,
-and central finite differences for the backward functions.
+RoPE against its complex-number form (rotation composes, depends only on the
+relative position, leaves V and position 0 alone), and central finite
+differences for the backward functions.
 
 Weights are passed in the mathematical orientation W [K, N] (``nn.Linear``'s
 weight transposed).
