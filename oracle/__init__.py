@@ -79,6 +79,8 @@ def _load():
             lib.coda_oracle_amax.restype = ctypes.c_double
             lib.coda_oracle_e4m3_fake_quant.argtypes = [_dp, _i64, _dp]
             lib.coda_oracle_e4m3_fake_quant.restype = ctypes.c_double
+            lib.coda_oracle_round_bf16_array.argtypes = [_dp, _i64, _dp]
+            lib.coda_oracle_round_bf16_array.restype = None
             lib.coda_oracle_rmsnorm_backward.argtypes = [_dp, _dp, ctypes.c_double, _dp, _i64, _i64, _dp, _dp]
             lib.coda_oracle_silu_mul_backward.argtypes = [_dp, _dp, _dp, _i64, _dp, _dp]
             lib.coda_oracle_threads.argtypes = [ctypes.c_int]
@@ -156,6 +158,14 @@ def e4m3_encode(x: float) -> int:
 
 def e4m3_decode(code: int) -> float:
     return float(_load().coda_oracle_e4m3_decode(int(code)))
+
+
+def round_bf16(x) -> np.ndarray:
+    """x rounded to the nearest bfloat16 value (ties to even), as fp64."""
+    x = _f64(x)
+    out = np.empty_like(x)
+    _load().coda_oracle_round_bf16_array(_ptr(x), x.size, _ptr(out))
+    return out
 
 
 def fake_quant_e4m3(x):
@@ -299,10 +309,17 @@ def chain_full_fp8(X, Wo, R, gamma1, Wg, Wu, Wd, gamma2, Wq, eps, out_rows=None)
     (gamma folded in first), h1, act and h2, each with its own per-tensor
     scale amax/448.  R, h, r and the outputs stay unquantised.
 
+    The quantiser reads each tensor as the block stores it, rounded to bf16:
+    the folded weights, h1, act and h2 (X and the weights arrive in bf16).
+    The write-up names FP8 operands but not the precision the quantiser reads;
+    an e4m3 code is a decision that a rounding of its input can flip, so it is
+    taken on the stored bf16 value, and so is amax, which sets every code's
+    scale.
+
     ``out_rows``: when given, every result is returned for those rows only and
     the last GEMM (Z) is computed for them alone.  The per-tensor scales still
     come from the whole tensors, so the values equal the full computation's."""
-    q = lambda t: fake_quant_e4m3(t)[0]
+    q = lambda t: fake_quant_e4m3(round_bf16(t))[0]
     g1, g2 = _f64(gamma1), _f64(gamma2)
     Wg_f = _f64(Wg) * g1[:, None]
     Wu_f = _f64(Wu) * g1[:, None]

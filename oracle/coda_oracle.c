@@ -137,6 +137,33 @@ uint8_t coda_oracle_e4m3_encode(double x)
     return sign | (uint8_t)(((e + 7) << 3) | (int)(q - 8.0));
 }
 
+/* Round to the nearest bfloat16 value, ties to even: 1 sign bit, 8 exponent
+ * bits (the fp32 range), 8 significant bits.  A value a in [2^(e-1), 2^e)
+ * lies on the grid k * 2^(e-8), k in [128, 256); below 2^-126 the grid is the
+ * subnormal one, multiples of 2^-133.  Magnitudes past the largest finite
+ * value, 255 * 2^120, round to infinity.  Zeros, infinities and NaNs pass. */
+double coda_oracle_round_bf16(double x)
+{
+    if (x == 0.0 || !isfinite(x))
+        return x;
+    int e;
+    (void)frexp(x, &e);                     /* |x| = f * 2^e, f in [0.5, 1) */
+    int ulp_e = e - 8;
+    if (ulp_e < -133)
+        ulp_e = -133;
+    const double y = ldexp(nearbyint(ldexp(x, -ulp_e)), ulp_e);  /* both scalings exact */
+    if (fabs(y) > ldexp(255.0, 120))
+        return copysign(INFINITY, x);
+    return y;
+}
+
+void coda_oracle_round_bf16_array(const double *x, int64_t n, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = coda_oracle_round_bf16(x[i]);
+}
+
 /* max_i |x_i| */
 double coda_oracle_amax(const double *x, int64_t n)
 {

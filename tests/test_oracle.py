@@ -35,13 +35,19 @@ def test_golden_rowscale(case):
 def test_golden_full_chain():
     c = next(c for c in GOLDEN["cases"] if c["kind"] == "full")
     args = [A(c[k]) for k in ("X", "Wo", "R", "gamma1", "Wg", "Wu", "Wd", "gamma2", "Wq")]
-    for fn in (oracle.chain_full, oracle.chain_full_fp8):
-        # every tensor of this case is exactly representable after per-tensor
-        # E4M3 scaling (a single nonzero magnitude per tensor), so the
-        # quantisation-aware chain must reproduce the exact values too
-        out = fn(*args, c["eps"])
-        for k in ("h1", "r1", "act", "h2", "r2", "Z"):
-            _close(out[k], c[k], 1e-12)
+    out = oracle.chain_full(*args, c["eps"])
+    for k in ("h1", "r1", "act", "h2", "r2", "Z"):
+        _close(out[k], c[k], 1e-12)
+    # every tensor of this case holds a single nonzero magnitude, so per-tensor
+    # E4M3 scaling represents it exactly and the quantisation-aware chain keeps
+    # the exact values, except that its quantiser reads act rounded to bf16:
+    # h2 and r2 move by at most that rounding (2^-9 relative), Z not at all
+    # (r2 cancels the magnitude of the one-row h2)
+    out = oracle.chain_full_fp8(*args, c["eps"])
+    for k in ("h1", "r1", "act", "Z"):
+        _close(out[k], c[k], 1e-12)
+    for k in ("h2", "r2"):
+        _close(out[k], c[k], 2.0 ** -9)
 
 
 def _fp8_case():
@@ -66,12 +72,13 @@ def _fp8_chain_variant(args, eps, skip=(), fold_after=False, quant_R=False, r_fr
     """The FP8 chain composed from the oracle's steps with one site moved, to
     show that the golden case above tells each misplacement apart."""
     X, Wo, R, g1, Wg, Wu, Wd, g2, Wq = args
-    q = lambda n, t: t if n in skip else oracle.fake_quant_e4m3(t)[0]  # noqa: E731
+    # the quantiser reads the bf16-rounded tensor, as the block stores it
+    q = lambda n, t: t if n in skip else oracle.fake_quant_e4m3(oracle.round_bf16(t))[0]  # noqa: E731
     if fold_after:
         Wg_f, Wu_f, Wq_f = g1[:, None] * q("Wg", Wg), g1[:, None] * q("Wu", Wu), g2[:, None] * q("Wq", Wq)
     else:
         Wg_f, Wu_f, Wq_f = q("Wg", g1[:, None] * Wg), q("Wu", g1[:, None] * Wu), q("Wq", g2[:, None] * Wq)
-    h1 = oracle.gemm(q("X", X), q("Wo", Wo), oracle.fake_quant_e4m3(R)[0] if quant_R else R)
+    h1 = oracle.gemm(q("X", X), q("Wo", Wo), oracle.fake_quant_e4m3(oracle.round_bf16(R))[0] if quant_R else R)
     h1q = q("h1", h1)
     _, r1 = oracle.rmsnorm(h1q if r_from_q else h1, g1, eps)
     act = oracle.silu_mul(oracle.gemm(h1q, Wg_f) * r1[:, None], oracle.gemm(h1q, Wu_f) * r1[:, None])
@@ -199,6 +206,28 @@ def test_e4m3_encode_vs_torch_rne():
     zero = (ref & 0x7F) == 0
     assert np.array_equal(got[~zero], ref[~zero])
     assert np.all((got[zero] & 0x7F) == 0)
+
+
+def test_round_bf16_vs_torch_and_hand_ties():
+    """bf16 rounding (the quantiser's input in the FP8 chain) against torch's
+    fp32 -> bf16 cast on fp32 values across the whole range, subnormals
+    included (exact in fp64, so both round once), and hand-worked ties."""
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2 ** 31, 200000, dtype=np.int64).astype(np.uint32)
+    x32 = bits.view(np.float32)
+    x32 = x32[np.isfinite(x32)]
+    # exact midpoints between neighbouring bf16 values: the 16 low bits 0x8000
+    ties = ((bits & np.uint32(0xFFFF0000)) | np.uint32(0x8000)).view(np.float32)
+    x32 = np.concatenate([x32, ties[np.isfinite(ties)], -x32[:1000]])
+    ref = torch.from_numpy(x32.copy()).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_bf16(x32.astype(np.float64))
+    assert np.array_equal(got, ref)
+    hand = {1 + 2.0 ** -8: 1.0, 1 + 3 * 2.0 ** -8: 1 + 2.0 ** -6, -(1 + 2.0 ** -8): -1.0, 0.3: 0.30078125,
+            2.0 ** -130: 2.0 ** -130, 3 * 2.0 ** -134: 2.0 ** -132, 2.0 ** -134: 0.0,
+            255 * 2.0 ** 120: 255 * 2.0 ** 120}
+    for v, want in hand.items():
+        assert oracle.round_bf16(np.array([v]))[0] == want, v
+    assert np.isinf(oracle.round_bf16(np.array([255.5 * 2.0 ** 120]))[0])  # a tie to 2^128: infinity
 
 
 def test_e4m3_saturates_and_nan():
