@@ -23,7 +23,8 @@ steps in the order the block applies them.
 Parity pins (tests/test_oracle.py): hand-derived 4x4 cases and a one-row chain
 in tests/golden/, numpy fp64 matmul on a C0-sized case, the reparameterisation
 identity, RMSNorm scale invariance, silu special values, the E4M3 codec
-against torch's float8_e4m3fn over all 256 codes, a hand-derived FP8 chain in
+against torch's float8_e4m3fn over all 256 codes, bf16 rounding against
+torch's fp32 -> bf16 cast and hand-worked ties, a hand-derived FP8 chain in
 which every quantisation site (and the fold before it) changes the result,
 RoPE against its complex-number form (rotation composes, depends only on the
 relative position, leaves V and position 0 alone), and central finite
