@@ -619,7 +619,7 @@ def run_coda(args, w):
     sets = [prepare_set(g, C, w, inp, dev, rank, s) for s in range(NSETS)]
     torch.cuda.synchronize()
     # FP8 defaults to the nine-launch chain: the FP8 blocks (one launch per
-    # block, quantisation in the launch) measured slower on GB300
+    # block, quantisation in the launch) measured up to 1% slower on GB300
     mode = args.reduce if args.reduce != "auto" else ("fused" if w.dtype == "e4m3" else "block")
     wksp = g.block_fp8_workspace(w.M, dev) if w.dtype == "e4m3" else g.block_workspace(w.M, dev)
     step, launches = make_step(g, C, w, mode, w.eps, wksp, args.fp8_x, args.fp8_act)
