@@ -190,10 +190,10 @@ constexpr int64_t kQuantPass = 32 * 16 * kQuantGroups;
 // fence waits for the warp's stores to land; paid once per pass, it kept the
 // quantiser warps waiting for most of their time (an in-launch pass over the
 // 8B chain's act ran 4.6x slower than the standalone quantise kernel), so a
-// chunk of several passes pays it once.  8 measured fastest of 1, 2, 4, 8;
-// larger chunks make a band complete later.
+// chunk of several passes pays it once.  16 measured fastest of 1, 2, 4, 8,
+// 16; larger chunks make a band complete later.
 #ifndef CODA_QUANT_PASSES
-#define CODA_QUANT_PASSES 8
+#define CODA_QUANT_PASSES 16
 #endif
 constexpr int kQuantPasses = CODA_QUANT_PASSES;
 constexpr int64_t kQuantChunk = kQuantPasses * kQuantPass;
@@ -487,10 +487,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   const int n_tiles_a = (pa.N_out + C::out_cols(C::kEpiA) - 1) / C::out_cols(C::kEpiA);
   const int n_tiles_b = C::TWO_PHASE ? (pb.N_out + C::out_cols(C::kEpiB) - 1) / C::out_cols(C::kEpiB) : 0;
   const int num_tiles = m_tiles * (n_tiles_a + n_tiles_b);
-  // phase-B rounds that units holding an extra phase-A tile sit out
-  const int b_rounds = C::TWO_PHASE ? ((pa.K + C::BK - 1) / C::BK + ((pb.K + C::BK - 1) / C::BK) / 2) /
-                                          max(1, (pb.K + C::BK - 1) / C::BK)
-                                    : 0;
+  // phase-B rounds that units holding an extra phase-A tile sit out.  An FP8
+  // block's phase B starts on every unit at once, after the grid-wide amax
+  // barrier, so there the phase-B tiles go plain round robin (sitting out
+  // rounds would leave the other units with 3-4 more tiles at the end).
+  const int b_rounds = (C::TWO_PHASE && !C::FP8_BLOCK)
+                           ? ((pa.K + C::BK - 1) / C::BK + ((pb.K + C::BK - 1) / C::BK) / 2) /
+                                 max(1, (pb.K + C::BK - 1) / C::BK)
+                           : 0;
   auto walk = [&](int k) { return walk_tile(unit, k, n_units, m_tiles * n_tiles_a, m_tiles * n_tiles_b, b_rounds); };
   // a band is ready for phase B when every phase-A tile of it (one increment
   // per CTA) has stored h and P
