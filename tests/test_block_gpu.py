@@ -119,3 +119,45 @@ def test_block_rejects_fp8_and_missing_workspace():
     ws = g.block_workspace(128, "cuda")
     with pytest.raises(g.CodaError, match="UNSUPPORTED"):
         g.coda_block_rowscale(X, W, R, W, 1e-5, ws, H=R.clone(), Z=R.clone())
+
+
+@pytest.mark.parametrize("cg", ["1", "2"])
+def test_blocks_replay_in_a_cuda_graph(cg, monkeypatch):
+    """The two one-launch blocks of the block tail captured once in a CUDA graph
+    and replayed: every replay equals the eager calls bit for bit, and each
+    launch leaves its workspace zeroed for the next, so replays need no reset."""
+    import gemm_epilogue_fusion_gb300 as g
+    from gemm_epilogue_fusion_gb300 import chain as C
+    monkeypatch.setenv("CODA_CTA_GROUP", cg)
+    w = Workload("graph_chain", "full", 700, 264, 392, 200, 576, "bf16", 1e-5, 61)
+    inp = make_inputs(w)
+    d = to_device(inp)
+    f = C.fold_weights("full", {k: d[k] for k in d if k.startswith("W")}, {k: d[k] for k in d if k.startswith("gamma")})
+    ws1, ws2 = g.block_workspace(w.M, "cuda"), g.block_workspace(w.M, "cuda")
+    M, H, I, Q = w.M, w.N, w.inter, w.N2
+    e = lambda *s, dt=torch.bfloat16: torch.empty(*s, dtype=dt, device="cuda")  # noqa: E731
+    out = {"h1": e(M, H), "P1": e(M, g.coda_partial_cols(H), dt=torch.float32), "act": e(M, I),
+           "h2": e(M, H), "P2": e(M, g.coda_partial_cols(H), dt=torch.float32), "Z": e(M, Q)}
+    s = torch.cuda.Stream()
+
+    def step():
+        g.coda_block_swiglu(d["X"], d["W1t"], d["R"], f["Wgt"], f["Wut"], w.eps, ws1, H=out["h1"], P=out["P1"],
+                            Act=out["act"], stream=s)
+        g.coda_block_rowscale(out["act"], d["Wdt"], out["h1"], f["Wqt"], w.eps, ws2, H=out["h2"], P=out["P2"],
+                              Z=out["Z"], stream=s)
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    eager = {k: v.clone() for k, v in out.items()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    for _ in range(3):
+        for v in out.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for k in out:
+            assert torch.equal(out[k], eager[k]), k
+        assert torch.count_nonzero(ws1).item() == 0 and torch.count_nonzero(ws2).item() == 0
